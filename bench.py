@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one pass of the whole path over one batch: the cache write of the
+step's new tokens (pa_reshape_and_cache) followed by paged decode attention
+(pa_decode_ex: decode kernel, plus the split-KV reduce when the plan splits).
+
+Default workload: the small GQA bf16 decode (64 sequences, 32 query / 8 KV
+heads, head size 64, lengths uniform in [1, 2048], 2 GiB pool of 65536 blocks,
+64 new tokens written per step).  ``--config c3|c4|c5`` measures the other
+configurations.  L2 is flushed (a 512 MiB write) before every timed step,
+outside the timed events.
+
+Prints one JSON line.  ``value`` = paged-decode KV-read GB/s over the whole step
+(algorithmic decode bytes / step time); ``roofline`` is for the decode kernel
+alone (profiling events on its launch stream); ``e2e`` repeats the step from
+pinned host buffers with the host<->device copies inside the timed region;
+``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same
+workload.  ``--impl reference`` times that oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import configs, data  # noqa: E402
+
+METRIC = "paged-decode KV-read GB/s (% of HBM peak), tokens/s; cache-write GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma16.cu", "pa_decode_mma_fp8.cu", "pa_decode.cu",
+                  "pa_device.cuh", "pa_internal.h", "pa_api.cu"]
+
+
+# ----------------------------------------------------------------- staging
+
+class Staged:
+    """Device-resident inputs and outputs of one workload."""
+
+
+def _torch_dt(name):
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}[name]
+
+
+def nan_fill_(t: torch.Tensor) -> None:
+    """Poison a cache with NaN bit patterns (all bytes 0xFF is NaN for fp32, bf16, f16, e4m3)."""
+    t.view(torch.uint8).fill_(0xFF)
+
+
+def stage(w, device="cuda", history=True, poison=True) -> Staged:
+    """Allocate the cache pool (NaN-poisoned), write the history rows through the library's own
+    cache write, and stage this step's new rows, metadata and output buffers on `device`."""
+    import paged_decode_attention_reshape_gb300 as pa
+    st = Staged()
+    st.w = w
+    cdt = _torch_dt(w.cache_dtype)
+    shape = (w.num_blocks, w.Hkv, configs.BLOCK, w.D)
+    st.k_cache = torch.empty(shape, dtype=cdt, device=device)
+    st.v_cache = torch.empty(shape, dtype=cdt, device=device)
+    if poison:
+        nan_fill_(st.k_cache)
+        nan_fill_(st.v_cache)
+    st.fp8 = w.kv_dtype == "e4m3"
+    st.kv_mode = pa.PA_KV_FP8_E4M3 if st.fp8 else pa.PA_KV_AUTO
+    st.k_scale = torch.tensor([w.k_scale], dtype=torch.float32, device=device)
+    st.v_scale = torch.tensor([w.v_scale], dtype=torch.float32, device=device)
+    st.err = torch.zeros(1, dtype=torch.int32, device=device)
+    bt = w.block_table.copy()
+    st.block_table = torch.from_numpy(bt).to(device)
+    st.seq_lens = torch.from_numpy(w.seq_lens.astype(np.int32)).to(device)
+    st.q = data.q(w, device)
+    st.out = torch.empty_like(st.q)
+    st.k_step, st.v_step = data.step_rows(w, device)
+    st.slot_mapping = torch.from_numpy(w.step_slot.astype(np.int64)).to(device)
+    if history:
+        write_history(st, device)
+    return st
+
+
+def write_history(st: Staged, device="cuda", rows_per_call=1 << 16) -> None:
+    """Every position [0, L_s) of every sequence gets its history row (the step overwrites some)."""
+    import paged_decode_attention_reshape_gb300 as pa
+    w = st.w
+    for s in range(w.S):
+        L = int(w.seq_lens[s])
+        for p0 in range(0, L, rows_per_call):
+            p1 = min(L, p0 + rows_per_call)
+            pos = torch.arange(p0, p1, dtype=torch.int64)
+            K, V = data.history_rows(w, s, device, positions=pos)
+            slots = torch.from_numpy(w.slot_of(s, np.arange(p0, p1))).to(device)
+            pa.pa_reshape_and_cache(K, V, st.k_cache, st.v_cache, slots, st.kv_mode, st.k_scale, st.v_scale,
+                                    st.err)
+    torch.cuda.synchronize()
+
+
+def workspace_for(st: Staged, partition_size: int):
+    import paged_decode_attention_reshape_gb300 as pa
+    w = st.w
+    code = {"f32": pa.PA_F32, "bf16": pa.PA_BF16, "e4m3": pa.PA_FP8_E4M3}[w.cache_dtype]
+    P, nparts = pa.pa_decode_plan(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, code, 0, partition_size)
+    nbytes = pa.pa_decode_workspace_size(w.S, w.Hq, w.D, w.max_blocks, P) if P > 0 else 0
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=st.q.device)
+    return P, nparts, ws
+
+
+def run_write(st: Staged) -> None:
+    import paged_decode_attention_reshape_gb300 as pa
+    pa.pa_reshape_and_cache(st.k_step, st.v_step, st.k_cache, st.v_cache, st.slot_mapping, st.kv_mode,
+                            st.k_scale, st.v_scale, st.err)
+
+
+def run_decode(st: Staged, partition_size: int = 0, ws=None, out=None) -> None:
+    import paged_decode_attention_reshape_gb300 as pa
+    w = st.w
+    pa.pa_decode_ex(st.out if out is None else out, st.q, st.k_cache, st.v_cache, st.block_table, st.seq_lens,
+                    w.scale, w.Hkv, st.k_scale if st.fp8 else None, st.v_scale if st.fp8 else None,
+                    partition_size, ws, st.err)
+
+
+def run_step(st: Staged, partition_size: int = 0, ws=None) -> None:
+    run_write(st)
+    run_decode(st, partition_size, ws)
+
+
+# ------------------------------------------------------------ measurement
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_decode_attention_reshape_gb300", "csrc")
+    for name in DECODE_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(config: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it was
+    taken at the current decode sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = decode_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == config and parts[1] == cur:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            self.uuid = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def mine(r):
+            return self.uuid is None or self.uuid in r[0] or r[0] in self.uuid
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1 and len(r) >= 9 and mine(r)]
+        if len(rows) < 3:
+            rows = [r for (t, r) in self.rows if len(r) >= 9 and mine(r)]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.nanmedian(sm)), "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": float(np.nanmax([num(r[3]) for r in rows]))}
+
+
+def time_steps(st, K, flush, partition_size, ws, profile=False):
+    """Per-step device time (ms) of K steps, L2 flushed before each (outside the events)."""
+    import paged_decode_attention_reshape_gb300 as pa
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if profile:
+        pa.pa_profile_read(pa.PA_KERNEL_WRITE)
+        pa.pa_profile_read(pa.PA_KERNEL_DECODE)
+        pa.pa_profile_read(pa.PA_KERNEL_REDUCE)
+        pa.pa_profile_enable(True)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        run_step(st, partition_size, ws)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    prof = None
+    if profile:
+        pa.pa_profile_enable(False)
+        prof = {k: pa.pa_profile_read(k) for k in (pa.PA_KERNEL_WRITE, pa.PA_KERNEL_DECODE, pa.PA_KERNEL_REDUCE)}
+    return [a.elapsed_time(b) for a, b in ev], prof
+
+
+def e2e_steps(st, K, flush, partition_size, ws):
+    """Same step fed from pinned host buffers: H2D of the step's inputs (q, new K/V rows,
+    slot_mapping, block_table, seq_lens) and D2H of the output inside the timed events."""
+    host = {name: getattr(st, name).cpu().pin_memory() for name in
+            ("q", "k_step", "v_step", "slot_mapping", "block_table", "seq_lens")}
+    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        for name, t in host.items():
+            getattr(st, name).copy_(t, non_blocking=True)
+        run_step(st, partition_size, ws)
+        out_h.copy_(st.out, non_blocking=True)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev], h2d, d2h
+
+
+def cpu_baseline(w, target_s=12.0, max_seqs=None):
+    """Time the fp64 CPU oracle (as it stands) on a bounded sample of the workload: the cache
+    write of the sampled sequences' step rows and the dense decode of all their query heads.
+    Threads: one oracle call per (sequence) at a time on every host core."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    cores = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(7)
+    order = rng.permutation(w.S)
+    qs = data.q(w, "cpu").float().double().numpy()
+
+    def prep(s):
+        K, V = data.logical_kv(w, int(s))
+        if w.kv_dtype == "e4m3":   # bf16 bit patterns; the oracle quantises them itself
+            return ("e4m3", K.view(torch.int16).numpy().view(np.uint16), V.view(torch.int16).numpy().view(np.uint16))
+        return ("plain", K.float().numpy().astype(np.float64), V.float().numpy().astype(np.float64))
+
+    def work(item):
+        s, (kind, K, V) = item
+        L = K.shape[0]
+        if kind == "e4m3":
+            ck = np.zeros((L, w.Hkv, w.D), dtype=np.uint8)
+            cv = np.zeros((L, w.Hkv, w.D), dtype=np.uint8)
+            oracle.write_flat(K, "bf16", np.arange(L), ck, "e4m3", w.k_scale)
+            oracle.write_flat(V, "bf16", np.arange(L), cv, "e4m3", w.v_scale)
+            K = oracle.cache_values(ck, "e4m3", w.k_scale)
+            V = oracle.cache_values(cv, "e4m3", w.v_scale)
+        oracle.dense_decode(qs[s], K, V, w.scale)
+        return L
+
+    # calibrate on one sequence, then size the sample to about target_s of wall time
+    first = int(order[0])
+    t = time.perf_counter()
+    item0 = (first, prep(first))
+    work(item0)
+    one = time.perf_counter() - t
+    n = int(max(1, min(w.S, (target_s * cores) / max(one, 1e-3))))
+    if max_seqs:
+        n = min(n, max_seqs)
+    sample = [int(x) for x in order[:n]]
+    items = [(s, prep(s)) for s in sample]
+    t = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(work, items))
+    dt = time.perf_counter() - t
+    nb = sum((int(w.seq_lens[s]) + 15) // 16 for s in sample)
+    bytes_ = nb * 16 * w.Hkv * w.D * w.cache_elem_bytes() * 2 + 2 * n * w.Hq * w.D * w.in_elem_bytes() + nb * 4 + n * 4
+    return {"value": bytes_ / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d of %d sequences (all %d query heads, fp64 dense decode%s), %.2f s"
+                      % (n, w.S, w.Hq, " + e4m3 quantisation" if w.kv_dtype == "e4m3" else "", dt),
+            "tokens_per_s": n / dt}
+
+
+# --------------------------------------------------------------------- main
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main_reference(args):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = configs.get(args.config)
+    budget = 150.0
+    per_step = max(1.0, min(6.0, budget / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, target_s=per_step / 3)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_baseline(w, target_s=per_step)
+        vals.append(r)
+    wall = time.perf_counter() - t0
+    v = float(np.median([r["value"] for r in vals]))
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wall / max(1, args.steps) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name + " " + _workload_desc(w), "l2": "n/a (CPU)"},
+            "cpu_baseline": {"kind": "oracle", "cores": vals[-1]["cores"], "sample": vals[-1]["sample"],
+                             "value": v, "unit": "GB/s"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _workload_desc(w):
+    return ("S=%d Hq=%d Hkv=%d D=%d %s cache=%s L=[%d..%d] blocks=%d write_rows=%d"
+            % (w.S, w.Hq, w.Hkv, w.D, w.dtype, w.cache_dtype, int(w.seq_lens.min()), int(w.seq_lens.max()),
+               w.num_blocks, w.T))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="c2", choices=sorted(configs.BUILDERS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="setup + a few steps only (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return main_reference(args)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import paged_decode_attention_reshape_gb300 as pa
+    pa.lib()
+    ws, rank, local = dist_setup()
+    dev = "cuda"
+    w = configs.get(args.config)
+    st = stage(w, dev)
+    P, nparts, wspace = workspace_for(st, args.partition_size)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        run_step(st, args.partition_size, wspace)
+    torch.cuda.synchronize()
+    if args.quick:
+        rc, bits = pa.pa_check_device_error(st.err)
+        if rc != 0:
+            raise SystemExit("device error %d bits %d" % (rc, bits))
+        print(json.dumps({"quick": True, "config": w.name, "partition": P}), flush=True)
+        return 0
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+        # soak: keep the GPU busy ~1 s so the sampled clocks are the loaded ones
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(20):
+                flush.zero_()
+                run_step(st, args.partition_size, wspace)
+            torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    step_ms, prof = time_steps(st, args.steps, flush, args.partition_size, wspace, profile=True)
+    t1 = time.time()
+    barrier(ws)
+    clocks = sampler.summary(t0 - 0.15, t1 + 0.15) if sampler else None
+    if sampler:
+        sampler.stop()
+    rc, bits = pa.pa_check_device_error(st.err)
+    if rc != 0:
+        raise SystemExit("device error word set: status %d bits %d" % (rc, bits))
+
+    ms = float(np.mean(step_ms))
+    ms = max_over_ranks(ms, ws)
+    dec_bytes = w.decode_bytes()
+    value = ws * dec_bytes / (ms * 1e-3) / 1e9
+    wr_ms, wr_n = prof[pa.PA_KERNEL_WRITE]
+    dk_ms, dk_n = prof[pa.PA_KERNEL_DECODE]
+    rd_ms, rd_n = prof[pa.PA_KERNEL_REDUCE]
+    dk_avg = dk_ms / max(1, dk_n)
+    peak, peak_src = _peaks()
+    achieved = dec_bytes / (dk_avg * 1e-3) / 1e9
+    launches = wr_n + dk_n + rd_n
+
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = e2e_steps(st, max(10, min(args.steps, 200)), flush, args.partition_size, wspace)
+        em = max_over_ranks(float(np.mean(e_ms)), ws)
+        e2e = {"value": ws * dec_bytes / (em * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": em}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.cache_dtype if w.cache_dtype != "auto" else w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name + " " + _workload_desc(w), "l2": "flushed (512 MiB write before each step)",
+                   "partition_tokens": P, "partitions_max": nparts, "parallelism": "replicas" if ws > 1 else "1 GPU"},
+        "pct_of_hbm_peak": 100.0 * value / peak,
+        "tokens_per_s": ws * w.S / (ms * 1e-3),
+        "decode_kernel_us": dk_avg * 1e3,
+        "reduce_kernel_us": rd_ms / max(1, rd_n) * 1e3 if rd_n else 0.0,
+        "cache_write": {"GB/s": w.write_bytes() / ((wr_ms / max(1, wr_n)) * 1e-3) / 1e9,
+                        "kernel_us": wr_ms / max(1, wr_n) * 1e3, "bytes": w.write_bytes()},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": _ncu_traffic(w.name), "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": dec_bytes, "kernel": "decode_mma_kernel"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

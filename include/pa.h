@@ -1,0 +1,222 @@
+/*
+ * pa.h -- C ABI of the GB300 paged KV-cache library (libpa_gb300.so).
+ *
+ * Two operations from the paged-attention pages, plus the plumbing around them:
+ *
+ *   pa_reshape_and_cache   write each new token's K/V rows into the physical
+ *                          cache block its slot_mapping entry names
+ *                          ("Inside vLLM CUDA Kernels: KV-Cache Writes and Paged
+ *                          Attention", Part 2; "How vLLM CUDA Kernels Write and
+ *                          Read the Paged KV Cache", "Writing K and V into the cache")
+ *   pa_decode / _ex        single-query paged decode attention with GQA, online
+ *                          softmax and split-KV partitions merged by a
+ *                          log-sum-exp reduce ("Inside vLLM CUDA Kernels", Part 3;
+ *                          "vLLM 源码完全拆解（七）", 参数与内存布局 through V1 与 V2)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are passed as pa_tensor descriptors: a data pointer, an element type,
+ *    a rank and per-dimension extents and strides (strides in ELEMENTS).  All data
+ *    pointers are DEVICE pointers on the current CUDA device unless a comment says
+ *    otherwise.  The caller owns all memory; the library keeps no pointer after a
+ *    call returns (pa_decode's internal workspace excepted, see below).
+ *  - The block size (tokens per KV-cache block) is fixed at PA_BLOCK_SIZE = 16.
+ *  - Cache layout ("HND"): k_cache and v_cache are each [num_blocks, num_kv_heads,
+ *    16, head_size], innermost dimension contiguous.  One (block, kv head) page is
+ *    16 x head_size elements; with the default contiguous strides it is one
+ *    contiguous run of memory.  Other strides for the two outer dimensions are
+ *    accepted (for instance K and V as views of one [num_blocks, 2, ...] tensor).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and never synchronise, except pa_check_device_error and
+ *    pa_profile_read.
+ *  - Return value: PA_OK (0) or a negative pa_status.  Argument errors are
+ *    detected on the host before anything is launched; nothing is written then.
+ *  - Faults that only the device can see (a slot, block id or sequence length out
+ *    of range) never cause an out-of-bounds access: the affected work item writes
+ *    nothing and sets a bit in the caller's device error word (when one is given),
+ *    which pa_check_device_error reports.
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_BLOCK_SIZE 16
+
+typedef enum {
+    PA_F32 = 0,
+    PA_BF16 = 1,
+    PA_F16 = 2,
+    PA_FP8_E4M3 = 3, /* OCP OFP8 E4M3: bias 7, no infinities, max 448 */
+    PA_I32 = 4,
+    PA_I64 = 5
+} pa_dtype;
+
+typedef enum {
+    PA_KV_AUTO = 0,     /* cache element type == key/value element type: bit copy */
+    PA_KV_FP8_E4M3 = 1  /* quantise to E4M3 with a per-tensor scale */
+} pa_kv_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,       /* null pointer, rank/extent mismatch, Hq % Hkv != 0 ... */
+    PA_ERR_UNSUPPORTED_DTYPE = -2, /* element type (combination) not provided */
+    PA_ERR_ALIGNMENT = -3,         /* a base pointer or stride breaks the 16-byte rule */
+    PA_ERR_WORKSPACE = -4,         /* workspace missing or smaller than required */
+    PA_ERR_CUDA = -5,              /* a CUDA runtime/driver call or launch failed */
+    PA_ERR_DEVICE_BOUNDS = -6,     /* device error word: slot / block id / length out of range */
+    PA_ERR_UNSUPPORTED_SHAPE = -7, /* head_size or block size outside what is built */
+    PA_ERR_DEVICE_TIMEOUT = -8     /* device error word: a bounded wait gave up */
+} pa_status;
+
+/* Bits of the device error word (an int in device memory, owned by the caller). */
+#define PA_DEVERR_SLOT_RANGE 0x1    /* slot_mapping entry >= num_blocks * 16 */
+#define PA_DEVERR_BLOCK_RANGE 0x2   /* block_table entry read < 0 or >= num_blocks */
+#define PA_DEVERR_SEQLEN_RANGE 0x4  /* seq_lens[s] < 0 or > max_blocks_per_seq * 16 */
+#define PA_DEVERR_WAIT_TIMEOUT 0x8  /* a shared-memory pipeline wait exceeded its limit */
+
+typedef void *pa_stream_t; /* cudaStream_t */
+
+typedef struct {
+    void *data;        /* device pointer to element [0, 0, ...] */
+    int32_t dtype;     /* pa_dtype */
+    int32_t ndim;      /* rank, 1..5 */
+    int64_t shape[5];  /* extents */
+    int64_t stride[5]; /* strides in elements */
+} pa_tensor;
+
+/*
+ * pa_reshape_and_cache -- scatter this step's new K/V rows into the paged cache.
+ *
+ * Defined by: "Inside vLLM CUDA Kernels", Part 2 (reshape_and_cache_flash: one
+ * destination slot per token, slot -> (block = slot / 16, offset = slot % 16),
+ * negative slot = padding with no destination; k_op = copy, or scale and convert
+ * for an FP8 cache).
+ *
+ *   key, value    [T, Hkv, D], PA_F32 / PA_BF16 / PA_F16 (same type for both);
+ *                 innermost stride 1; the token and head strides are free.
+ *   k_cache,      [num_blocks, Hkv, 16, D]; element type == key's for PA_KV_AUTO,
+ *   v_cache       PA_FP8_E4M3 for PA_KV_FP8_E4M3.  Written in place.
+ *   slot_mapping  PA_I64 [T].  Row t goes to cache slot slot_mapping[t];
+ *                 a negative entry writes nothing for row t.  Entries
+ *                 >= num_blocks * 16 write nothing and set PA_DEVERR_SLOT_RANGE.
+ *                 Two rows naming the same slot: which one lands is unspecified.
+ *   kv_dtype      PA_KV_AUTO: bit-exact copy.  PA_KV_FP8_E4M3: each element x is
+ *                 stored as E4M3(fp32(x) / scale) -- one IEEE fp32 division
+ *                 rounded to nearest, then round-to-nearest-even to E4M3 with
+ *                 saturation to +-448 and NaN -> 0x7F.
+ *   k_scale,      device pointers to one fp32 scale each (per tensor); NULL means
+ *   v_scale       1.0.  Ignored for PA_KV_AUTO.
+ *   device_error  device int to OR error bits into, or NULL.
+ * Alignment: key/value/cache base pointers and all strides in bytes must be
+ * multiples of 16 bytes, and D * element size a multiple of 16.
+ * T == 0 is a no-op.
+ */
+int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache,
+                         pa_tensor *v_cache, const pa_tensor *slot_mapping, int kv_dtype,
+                         const float *k_scale, const float *v_scale, int *device_error,
+                         pa_stream_t stream);
+
+/*
+ * pa_decode -- single-query paged decode attention (one query token per sequence).
+ *
+ * Defined by: "Inside vLLM CUDA Kernels", Part 3 (scores = q k^T * scale,
+ * softmax, probs v; online softmax m/l/acc; split-KV merged by max/LSE
+ * rescaling) and "vLLM 源码完全拆解（七）" (query [num_seqs, num_heads,
+ * head_size]; block_table walk over the first ceil(seq_len / 16) entries; GQA map
+ * kv_head = q_head / (Hq / Hkv); tail tokens t >= seq_len excluded from max and
+ * denominator; stale tail values never reach the output).
+ *
+ *   out           [S, Hq, D], same element type as q (may be the same memory as q).
+ *   q             [S, Hq, D], PA_F32 / PA_BF16 / PA_F16, innermost stride 1.
+ *   k_cache,      [num_blocks, Hkv, 16, D]; element type == q's, or PA_FP8_E4M3
+ *   v_cache       with a PA_BF16 / PA_F16 query.
+ *   block_table   PA_I32 [S, max_blocks_per_seq], innermost stride 1.  Only the
+ *                 first ceil(seq_lens[s] / 16) entries of row s are read.
+ *   seq_lens      PA_I32 [S]: visible KV length of each sequence, counting the
+ *                 token written in this step.  0 gives an all-zero output row.
+ *   scale         softmax scale (usually 1 / sqrt(D)).
+ *   num_kv_heads  Hkv; must equal k_cache->shape[1] and divide Hq.
+ * Head sizes built: 64, 128, 256 (FP8 caches: 128, 256).
+ * Uses a library-held workspace on the current device (grown on demand with
+ * cudaMallocAsync on `stream`); calls that use it on different streams must not
+ * overlap.  FP8 scales are 1.0 here; use pa_decode_ex for scales, a caller-owned
+ * workspace, an explicit partition size or a device error word.
+ */
+int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+              const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+              pa_stream_t stream);
+
+/*
+ * pa_decode_ex -- pa_decode with every knob.
+ *
+ *   k_scale, v_scale  device fp32 per-tensor dequantisation scales for an FP8 cache
+ *                     (K and V element values are code_value * scale); NULL = 1.0.
+ *   partition_size    KV tokens per split-KV partition: 0 = chosen by the
+ *                     library's measured heuristic (pa_decode_plan), -1 = never
+ *                     split, > 0 = that many tokens (rounded up to a multiple of 16).
+ *   workspace,        device memory for split-KV partial states; at least
+ *   workspace_bytes   pa_decode_workspace_size(...) bytes for the partition size
+ *                     the call ends up using (0 bytes when it does not split).
+ *                     NULL with workspace_bytes == 0 is fine for the unsplit path.
+ *   device_error      device int to OR error bits into, or NULL.
+ */
+int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                 const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                 const float *k_scale, const float *v_scale, int partition_size, void *workspace,
+                 size_t workspace_bytes, int *device_error, pa_stream_t stream);
+
+/*
+ * pa_decode_plan -- host-only: the partition size pa_decode_ex would use.
+ *   kv_dtype_code   pa_dtype of the cache; sm_count <= 0 queries the current device.
+ *   partition_size  in: as for pa_decode_ex.  *partition_out: tokens per partition
+ *                   (0 = unsplit); *num_partitions_out: partitions of the longest
+ *                   possible sequence (max_blocks_per_seq * 16 tokens).
+ * Returns PA_OK or PA_ERR_INVALID_ARG.  No device memory is touched.
+ */
+int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_blocks_per_seq,
+                   int kv_dtype_code, int sm_count, int partition_size, int *partition_out,
+                   int *num_partitions_out);
+
+/*
+ * pa_decode_workspace_size -- bytes of split-KV workspace for `partition_size`
+ * tokens per partition (0 or -1 = unsplit -> 0 bytes).  Host-only.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_size, int max_blocks_per_seq,
+                                int partition_size);
+
+/*
+ * pa_check_device_error -- synchronise `stream`, read the device error word,
+ * store its bits in *bits_out (nullable) and reset the word to 0.
+ * Returns PA_OK, PA_ERR_DEVICE_BOUNDS (any range bit), PA_ERR_DEVICE_TIMEOUT
+ * (wait bit only) or PA_ERR_CUDA.
+ */
+int pa_check_device_error(int *device_error, int *bits_out, pa_stream_t stream);
+
+/* Human-readable text for a pa_status value (static storage). */
+const char *pa_status_string(int status);
+
+/*
+ * Profiling: when enabled, every kernel the library launches is bracketed by a
+ * pair of CUDA events recorded on its launch stream.  pa_profile_read
+ * synchronises on the recorded events, returns the summed device time (ms) and
+ * the launch count for one kernel kind since the last read, and clears them.
+ *   kind: 0 = cache write, 1 = decode (the attention kernel itself),
+ *         2 = split-KV reduce.
+ */
+#define PA_KERNEL_WRITE 0
+#define PA_KERNEL_DECODE 1
+#define PA_KERNEL_REDUCE 2
+int pa_profile_enable(int on);
+int pa_profile_read(int kind, double *total_ms, long long *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_GB300_H */

@@ -1,0 +1,194 @@
+"""Python binding of libpa_gb300.so (include/pa.h): argument marshalling only.
+
+Every function here turns torch tensors into ``pa_tensor`` descriptors (data
+pointer, element type, extents, strides) and calls the C ABI function of the
+same name on the current CUDA stream.  No computation happens in Python, and
+there is no fallback: if the library is not built, importing works but the
+first call raises ``RuntimeError``.
+
+Element types: float32, bfloat16, float16; E4M3 caches as torch.uint8 (raw
+codes) or torch.float8_e4m3fn; block tables and sequence lengths int32;
+slot_mapping int64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa_gb300.so")
+
+PA_F32, PA_BF16, PA_F16, PA_FP8_E4M3, PA_I32, PA_I64 = range(6)
+PA_KV_AUTO, PA_KV_FP8_E4M3 = 0, 1
+PA_KERNEL_WRITE, PA_KERNEL_DECODE, PA_KERNEL_REDUCE = 0, 1, 2
+PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_SEQLEN_RANGE, PA_DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
+STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED_DTYPE", -3: "PA_ERR_ALIGNMENT",
+          -4: "PA_ERR_WORKSPACE", -5: "PA_ERR_CUDA", -6: "PA_ERR_DEVICE_BOUNDS", -7: "PA_ERR_UNSUPPORTED_SHAPE",
+          -8: "PA_ERR_DEVICE_TIMEOUT"}
+
+EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_ex", "pa_decode_plan", "pa_decode_workspace_size",
+           "pa_check_device_error", "pa_status_string", "pa_profile_enable", "pa_profile_read")
+
+_DT = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16, torch.uint8: PA_FP8_E4M3,
+       torch.int32: PA_I32, torch.int64: PA_I64}
+if hasattr(torch, "float8_e4m3fn"):
+    _DT[torch.float8_e4m3fn] = PA_FP8_E4M3
+
+
+class PaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 5), ("stride", ctypes.c_int64 * 5)]
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (where, STATUS.get(status, status), status_string(status)))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpa_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libpa_gb300.so is not built (expected at %s); run "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            P, T = ctypes.c_void_p, ctypes.POINTER(PaTensor)
+            i32, f32 = ctypes.c_int, ctypes.c_float
+            L.pa_reshape_and_cache.restype = i32
+            L.pa_reshape_and_cache.argtypes = [T, T, T, T, T, i32, P, P, P, P]
+            L.pa_decode.restype = i32
+            L.pa_decode.argtypes = [T, T, T, T, T, T, f32, i32, P]
+            L.pa_decode_ex.restype = i32
+            L.pa_decode_ex.argtypes = [T, T, T, T, T, T, f32, i32, P, P, i32, P, ctypes.c_size_t, P, P]
+            L.pa_decode_plan.restype = i32
+            L.pa_decode_plan.argtypes = [i32] * 8 + [ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            L.pa_decode_workspace_size.restype = ctypes.c_size_t
+            L.pa_decode_workspace_size.argtypes = [i32] * 5
+            L.pa_check_device_error.restype = i32
+            L.pa_check_device_error.argtypes = [P, ctypes.POINTER(i32), P]
+            L.pa_status_string.restype = ctypes.c_char_p
+            L.pa_status_string.argtypes = [i32]
+            L.pa_profile_enable.restype = i32
+            L.pa_profile_enable.argtypes = [i32]
+            L.pa_profile_read.restype = i32
+            L.pa_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().pa_status_string(int(status)).decode()
+    except RuntimeError:
+        return STATUS.get(status, "unknown")
+
+
+def desc(t: torch.Tensor, dtype_code: int | None = None) -> PaTensor:
+    """pa_tensor for a torch tensor (no copy)."""
+    if t.dim() > 5:
+        raise ValueError("rank > 5")
+    d = PaTensor()
+    d.data = t.data_ptr() if t.numel() else 0
+    d.dtype = _DT[t.dtype] if dtype_code is None else dtype_code
+    d.ndim = t.dim()
+    for i, (n, s) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = n
+        d.stride[i] = s
+    return d
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise PAError(rc, where)
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, kv_dtype: int = PA_KV_AUTO,
+                         k_scale=None, v_scale=None, device_error=None, stream=None) -> None:
+    """Scatter key/value [T, Hkv, D] rows into k_cache/v_cache [NB, Hkv, 16, D] at slot_mapping [T] (int64).
+    kv_dtype PA_KV_FP8_E4M3 quantises with the device fp32 scales k_scale/v_scale (1-element tensors)."""
+    args = (desc(key), desc(value), desc(k_cache), desc(v_cache), desc(slot_mapping))
+    rc = lib().pa_reshape_and_cache(*[ctypes.byref(a) for a in args], int(kv_dtype), _ptr(k_scale), _ptr(v_scale),
+                                    _ptr(device_error), _stream(stream))
+    _check(rc, "pa_reshape_and_cache")
+
+
+def pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, num_kv_heads: int,
+              stream=None) -> None:
+    """Paged decode attention: out/q [S, Hq, D], caches [NB, Hkv, 16, D], block_table [S, maxNB] int32,
+    seq_lens [S] int32."""
+    args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(block_table), desc(seq_lens))
+    rc = lib().pa_decode(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), _stream(stream))
+    _check(rc, "pa_decode")
+
+
+def pa_decode_ex(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, num_kv_heads: int,
+                 k_scale=None, v_scale=None, partition_size: int = 0, workspace=None, device_error=None,
+                 stream=None) -> None:
+    """pa_decode with FP8 scales, explicit partition size (0 heuristic, -1 unsplit), caller workspace
+    (a uint8 CUDA tensor) and device error word (int32 CUDA tensor)."""
+    args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(block_table), desc(seq_lens))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().pa_decode_ex(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), _ptr(k_scale),
+                            _ptr(v_scale), int(partition_size), _ptr(workspace), ws_bytes, _ptr(device_error),
+                            _stream(stream))
+    _check(rc, "pa_decode_ex")
+
+
+def pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kv_dtype_code,
+                   sm_count=0, partition_size=0):
+    """(partition tokens or 0 for unsplit, partitions of the longest sequence) -- host only."""
+    P, n = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kv_dtype_code,
+                              sm_count, partition_size, ctypes.byref(P), ctypes.byref(n))
+    _check(rc, "pa_decode_plan")
+    return P.value, n.value
+
+
+def pa_decode_workspace_size(num_seqs, num_heads, head_size, max_blocks_per_seq, partition_size) -> int:
+    return int(lib().pa_decode_workspace_size(num_seqs, num_heads, head_size, max_blocks_per_seq, partition_size))
+
+
+def pa_check_device_error(device_error, stream=None):
+    """(status, bits); synchronises the stream and resets the word."""
+    bits = ctypes.c_int(0)
+    rc = lib().pa_check_device_error(_ptr(device_error), ctypes.byref(bits), _stream(stream))
+    return rc, bits.value
+
+
+def pa_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def pa_profile_enable(on: bool = True) -> None:
+    _check(lib().pa_profile_enable(1 if on else 0), "pa_profile_enable")
+
+
+def pa_profile_read(kind: int):
+    """(total device ms, launches) for kind PA_KERNEL_WRITE / _DECODE / _REDUCE since the last read."""
+    ms, n = ctypes.c_double(0), ctypes.c_longlong(0)
+    _check(lib().pa_profile_read(int(kind), ctypes.byref(ms), ctypes.byref(n)), "pa_profile_read")
+    return ms.value, n.value

@@ -1,0 +1,525 @@
+// pa_api.cu -- the C ABI of include/pa.h: argument validation, the split-KV
+// partition plan, TMA descriptors, workspace, device error word and profiling.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "pa_internal.h"
+
+#define PA_API extern "C" __attribute__((visibility("default")))
+
+namespace pa {
+namespace {
+
+// ------------------------------------------------------------------ helpers
+
+int elem_bytes(int dt) {
+  switch (dt) {
+    case PA_F32: case PA_I32: return 4;
+    case PA_BF16: case PA_F16: return 2;
+    case PA_FP8_E4M3: return 1;
+    case PA_I64: return 8;
+    default: return 0;
+  }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Descriptor sanity: non-null, rank, element type, positive extents.
+int check_desc(const pa_tensor *t, int ndim) {
+  if (!t || t->ndim != ndim) return PA_ERR_INVALID_ARG;
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0 || t->stride[i] < 0) return PA_ERR_INVALID_ARG;
+  if (elem_bytes(t->dtype) == 0) return PA_ERR_UNSUPPORTED_DTYPE;
+  return PA_OK;
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+// --------------------------------------------------------------- profiling
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[3];
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+Profiler &prof() {
+  static Profiler P;
+  return P;
+}
+
+// Brackets one kernel launch with events when profiling is on.
+struct ProfScope {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  ProfScope(int k, cudaStream_t s) : kind(k), st(s) {
+    Profiler &P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    if (!P.on) return;
+    e0 = P.get();
+    e1 = P.get();
+    cudaEventRecord(e0, st);
+  }
+  ~ProfScope() {
+    if (!e0) return;
+    cudaEventRecord(e1, st);
+    Profiler &P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    P.ev[kind].emplace_back(e0, e1);
+  }
+};
+
+// ------------------------------------------------------------- tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 4-D map over a [NB, Hkv, 16, D] cache: dims (D, 16, Hkv, NB), box (128 bytes, 16, 1, 1),
+// 128-byte swizzle.  One box = 16 token rows x 128 bytes = 2 KiB of one page.
+int make_cache_map(const pa_tensor *c, CUtensorMap *map) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PA_ERR_CUDA;
+  const int eb = elem_bytes(c->dtype);
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(c->shape[3]), static_cast<cuuint64_t>(c->shape[2]),
+                              static_cast<cuuint64_t>(c->shape[1]), static_cast<cuuint64_t>(c->shape[0])};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(c->stride[2] * eb), static_cast<cuuint64_t>(c->stride[1] * eb),
+                                 static_cast<cuuint64_t>(c->stride[0] * eb)};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 16, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  CUresult r = enc(map, dt, 4, c->data, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// --------------------------------------------------------------- plan
+
+int kind_of(int q_dtype, int cache_dtype) {
+  if (cache_dtype == PA_FP8_E4M3) {
+    if (q_dtype == PA_BF16) return KIND_FP8_BF16Q;
+    if (q_dtype == PA_F16) return KIND_FP8_F16Q;
+    return -1;
+  }
+  if (q_dtype != cache_dtype) return -1;
+  if (q_dtype == PA_BF16) return KIND_BF16;
+  if (q_dtype == PA_F16) return KIND_F16;
+  if (q_dtype == PA_F32) return KIND_F32;
+  return -1;
+}
+
+int ctas_per_sm(int kind, int D) {
+  if (kind == KIND_F32) return 4;
+  const size_t smem = mma_smem(kind, D);
+  int n = static_cast<int>((227u * 1024u) / (smem + 1024));
+  return std::max(1, std::min(n, 16));
+}
+
+// Partition size in tokens (0 = unsplit).  Without reading seq_lens (no host
+// sync), the plan sizes partitions from the block-table width: split only when
+// the (sequence, kv head, head group) units alone cannot fill the GPU, and
+// then cut the longest possible sequence into enough partitions for about four
+// resident waves, never below 256 tokens per partition.
+int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, int request) {
+  if (request < 0) return 0;
+  const int max_tokens = maxNB * kBlock;
+  int P;
+  if (request > 0) {
+    P = (request + kBlock - 1) / kBlock * kBlock;
+  } else {
+    const int G = Hq / Hkv;
+    const int64_t units = static_cast<int64_t>(S) * Hkv * ((G + 7) / 8);
+    const int64_t resident = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D);
+    if (units >= 2 * resident) return 0;
+    const int64_t parts = (4 * resident + units - 1) / units;
+    int64_t pages = (maxNB + parts - 1) / parts;
+    pages = std::max<int64_t>(pages, 16);
+    P = static_cast<int>(pages * kBlock);
+  }
+  if (P >= max_tokens) return 0;
+  return P;
+}
+
+size_t workspace_bytes_for(int S, int Hq, int D, int maxNB, int P) {
+  if (P <= 0) return 0;
+  const int64_t parts = (static_cast<int64_t>(maxNB) * kBlock + P - 1) / P;
+  const int64_t rows = static_cast<int64_t>(S) * Hq * parts;
+  const size_t ml = (static_cast<size_t>(rows) * sizeof(float2) + 255) & ~static_cast<size_t>(255);
+  return ml + static_cast<size_t>(rows) * D * sizeof(float);
+}
+
+// ------------------------------------------------------ internal workspace
+
+struct DevWorkspace {
+  void *ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+DevWorkspace g_ws[64];
+
+// ------------------------------------------------------------- validation
+
+int validate_cache_pair(const pa_tensor *kc, const pa_tensor *vc, int *NB, int *Hkv, int *D) {
+  int r;
+  if ((r = check_desc(kc, 4)) || (r = check_desc(vc, 4))) return r;
+  for (int i = 0; i < 4; ++i)
+    if (kc->shape[i] != vc->shape[i]) return PA_ERR_INVALID_ARG;
+  if (kc->dtype != vc->dtype) return PA_ERR_INVALID_ARG;
+  if (kc->shape[2] != kBlock) return PA_ERR_UNSUPPORTED_SHAPE;
+  if (kc->stride[3] != 1 || vc->stride[3] != 1) return PA_ERR_INVALID_ARG;
+  if (!kc->data || !vc->data) return PA_ERR_INVALID_ARG;
+  const int eb = elem_bytes(kc->dtype);
+  if (!aligned16(kc->data) || !aligned16(vc->data)) return PA_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i)
+    if ((kc->stride[i] * eb) % 16 || (vc->stride[i] * eb) % 16) return PA_ERR_ALIGNMENT;
+  if (kc->shape[0] > INT32_MAX || kc->shape[1] > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
+  *NB = static_cast<int>(kc->shape[0]);
+  *Hkv = static_cast<int>(kc->shape[1]);
+  *D = static_cast<int>(kc->shape[3]);
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+// ===================================================================== ABI
+
+PA_API const char *pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED_DTYPE: return "unsupported element type";
+    case PA_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case PA_ERR_CUDA: return "CUDA call or launch failed";
+    case PA_ERR_DEVICE_BOUNDS: return "device reported an out-of-range slot, block id or sequence length";
+    case PA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (block size, head size or extent)";
+    case PA_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+PA_API int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache, pa_tensor *v_cache,
+                                const pa_tensor *slot_mapping, int kv_dtype, const float *k_scale,
+                                const float *v_scale, int *device_error, pa_stream_t stream) {
+  int r;
+  if ((r = check_desc(key, 3)) || (r = check_desc(value, 3)) || (r = check_desc(slot_mapping, 1))) return r;
+  int NB, Hkv, D;
+  if ((r = validate_cache_pair(k_cache, v_cache, &NB, &Hkv, &D))) return r;
+  const int in_dt = key->dtype;
+  if (value->dtype != in_dt) return PA_ERR_INVALID_ARG;
+  if (in_dt != PA_F32 && in_dt != PA_BF16 && in_dt != PA_F16) return PA_ERR_UNSUPPORTED_DTYPE;
+  if (slot_mapping->dtype != PA_I64) return PA_ERR_UNSUPPORTED_DTYPE;
+  if (kv_dtype == PA_KV_AUTO) {
+    if (k_cache->dtype != in_dt) return PA_ERR_UNSUPPORTED_DTYPE;
+  } else if (kv_dtype == PA_KV_FP8_E4M3) {
+    if (k_cache->dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED_DTYPE;
+  } else {
+    return PA_ERR_INVALID_ARG;
+  }
+  const int64_t T = key->shape[0];
+  if (value->shape[0] != T || slot_mapping->shape[0] != T) return PA_ERR_INVALID_ARG;
+  if (key->shape[1] != Hkv || key->shape[2] != D || value->shape[1] != Hkv || value->shape[2] != D)
+    return PA_ERR_INVALID_ARG;
+  if (key->stride[2] != 1 || value->stride[2] != 1 || slot_mapping->stride[0] != 1) return PA_ERR_INVALID_ARG;
+  const int ib = elem_bytes(in_dt);
+  if ((static_cast<int64_t>(D) * ib) % 16) return PA_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return PA_OK;
+  if (!key->data || !value->data || !slot_mapping->data) return PA_ERR_INVALID_ARG;
+  if (!aligned16(key->data) || !aligned16(value->data)) return PA_ERR_ALIGNMENT;
+  for (int i = 0; i < 2; ++i)
+    if ((key->stride[i] * ib) % 16 || (value->stride[i] * ib) % 16) return PA_ERR_ALIGNMENT;
+
+  WriteParams p;
+  p.key = key->data;
+  p.value = value->data;
+  p.k_cache = k_cache->data;
+  p.v_cache = v_cache->data;
+  p.slot_mapping = static_cast<const int64_t *>(slot_mapping->data);
+  p.T = T;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.key_ts = key->stride[0];
+  p.key_hs = key->stride[1];
+  p.val_ts = value->stride[0];
+  p.val_hs = value->stride[1];
+  p.kc_s0 = k_cache->stride[0];
+  p.kc_s1 = k_cache->stride[1];
+  p.kc_s2 = k_cache->stride[2];
+  p.vc_s0 = v_cache->stride[0];
+  p.vc_s1 = v_cache->stride[1];
+  p.vc_s2 = v_cache->stride[2];
+  p.num_slots = static_cast<int64_t>(NB) * kBlock;
+  p.k_scale = kv_dtype == PA_KV_FP8_E4M3 ? k_scale : nullptr;
+  p.v_scale = kv_dtype == PA_KV_FP8_E4M3 ? v_scale : nullptr;
+  p.err = device_error;
+  const int sm = device_sm_count();
+  if (sm <= 0) return PA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  {
+    ProfScope ps(PA_KERNEL_WRITE, st);
+    e = launch_write(p, in_dt, k_cache->dtype, sm, st);
+  }
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_blocks_per_seq,
+                          int kv_dtype_code, int sm_count, int partition_size, int *partition_out,
+                          int *num_partitions_out) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size <= 0 ||
+      max_blocks_per_seq < 0)
+    return PA_ERR_INVALID_ARG;
+  int kind;
+  switch (kv_dtype_code) {
+    case PA_FP8_E4M3: kind = KIND_FP8_BF16Q; break;
+    case PA_BF16: kind = KIND_BF16; break;
+    case PA_F16: kind = KIND_F16; break;
+    case PA_F32: kind = KIND_F32; break;
+    default: return PA_ERR_INVALID_ARG;
+  }
+  if (sm_count <= 0) sm_count = device_sm_count();
+  if (sm_count <= 0) return PA_ERR_CUDA;
+  const int P = plan_partition(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kind, sm_count,
+                               partition_size);
+  if (partition_out) *partition_out = P;
+  if (num_partitions_out)
+    *num_partitions_out = P > 0 ? (max_blocks_per_seq * kBlock + P - 1) / P : 1;
+  return PA_OK;
+}
+
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_size, int max_blocks_per_seq,
+                                       int partition_size) {
+  if (num_seqs < 0 || num_heads < 0 || head_size < 0 || max_blocks_per_seq < 0) return 0;
+  const int P = partition_size > 0 ? (partition_size + kBlock - 1) / kBlock * kBlock : 0;
+  if (P >= max_blocks_per_seq * kBlock) return 0;
+  return workspace_bytes_for(num_seqs, num_heads, head_size, max_blocks_per_seq, P);
+}
+
+namespace {
+
+int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                const float *k_scale, const float *v_scale, int partition_size, void *workspace,
+                size_t workspace_bytes, bool internal_ws, int *device_error, pa_stream_t stream) {
+  int r;
+  if ((r = check_desc(out, 3)) || (r = check_desc(q, 3)) || (r = check_desc(block_table, 2)) ||
+      (r = check_desc(seq_lens, 1)))
+    return r;
+  int NB, Hkv, D;
+  if ((r = validate_cache_pair(k_cache, v_cache, &NB, &Hkv, &D))) return r;
+  const int64_t S64 = q->shape[0], Hq64 = q->shape[1];
+  if (num_kv_heads != Hkv || Hkv <= 0 || Hq64 <= 0 || Hq64 % Hkv) return PA_ERR_INVALID_ARG;
+  if (q->shape[2] != D) return PA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (out->shape[i] != q->shape[i]) return PA_ERR_INVALID_ARG;
+  if (out->dtype != q->dtype) return PA_ERR_INVALID_ARG;
+  if (block_table->dtype != PA_I32 || seq_lens->dtype != PA_I32) return PA_ERR_UNSUPPORTED_DTYPE;
+  if (block_table->shape[0] != S64 || seq_lens->shape[0] != S64) return PA_ERR_INVALID_ARG;
+  if (block_table->stride[1] != 1 || seq_lens->stride[0] != 1 || q->stride[2] != 1 || out->stride[2] != 1)
+    return PA_ERR_INVALID_ARG;
+  const int kind = kind_of(q->dtype, k_cache->dtype);
+  if (kind < 0) return PA_ERR_UNSUPPORTED_DTYPE;
+  if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED_SHAPE;
+  if ((kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) && D < 128) return PA_ERR_UNSUPPORTED_SHAPE;
+  if (S64 > 65535 || Hq64 > 65535 || block_table->shape[1] > (INT32_MAX / kBlock)) return PA_ERR_UNSUPPORTED_SHAPE;
+  if (S64 == 0) return PA_OK;
+  if (!q->data || !out->data || !block_table->data || !seq_lens->data) return PA_ERR_INVALID_ARG;
+  const int qb = elem_bytes(q->dtype);
+  if (!aligned16(q->data) || !aligned16(out->data)) return PA_ERR_ALIGNMENT;
+  for (int i = 0; i < 2; ++i)
+    if ((q->stride[i] * qb) % 16 || (out->stride[i] * qb) % 16) return PA_ERR_ALIGNMENT;
+
+  const int S = static_cast<int>(S64), Hq = static_cast<int>(Hq64);
+  const int maxNB = static_cast<int>(block_table->shape[1]);
+  const int sm = device_sm_count();
+  if (sm <= 0) return PA_ERR_CUDA;
+  const int P = plan_partition(S, Hq, Hkv, D, maxNB, kind, sm, partition_size);
+  const int max_parts = P > 0 ? (maxNB * kBlock + P - 1) / P : 1;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  DecodeParams p{};
+  p.out = out->data;
+  p.q = q->data;
+  p.out_ss = out->stride[0];
+  p.out_hs = out->stride[1];
+  p.q_ss = q->stride[0];
+  p.q_hs = q->stride[1];
+  p.block_table = static_cast<const int32_t *>(block_table->data);
+  p.bt_ss = block_table->stride[0];
+  p.seq_lens = static_cast<const int32_t *>(seq_lens->data);
+  p.S = S;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.HG = (p.G + 7) / 8;
+  p.D = D;
+  p.num_blocks = NB;
+  p.max_blocks = maxNB;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.pages_per_part = P > 0 ? P / kBlock : std::max(maxNB, 1);
+  p.max_parts = max_parts;
+  p.err = device_error;
+  if (kind != KIND_FP8_BF16Q && kind != KIND_FP8_F16Q) p.k_scale = p.v_scale = nullptr;
+  if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
+
+  if (max_parts > 1) {
+    const size_t need = workspace_bytes_for(S, Hq, D, maxNB, P);
+    if (internal_ws) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+      std::lock_guard<std::mutex> g(g_ws_mu);
+      DevWorkspace &w = g_ws[dev];
+      if (w.bytes < need) {
+        if (w.ptr) cudaFreeAsync(w.ptr, st);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (cudaMallocAsync(&w.ptr, need, st) != cudaSuccess) return PA_ERR_CUDA;
+        w.bytes = need;
+      }
+      workspace = w.ptr;
+      workspace_bytes = w.bytes;
+    }
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PA_ERR_ALIGNMENT;
+    const int64_t rows = static_cast<int64_t>(S) * Hq * max_parts;
+    const size_t ml = (static_cast<size_t>(rows) * sizeof(float2) + 255) & ~static_cast<size_t>(255);
+    p.part_ml = static_cast<float2 *>(workspace);
+    p.part_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + ml);
+  }
+
+  cudaError_t e;
+  if (kind == KIND_F32) {
+    p.kc = static_cast<const float *>(k_cache->data);
+    p.vc = static_cast<const float *>(v_cache->data);
+    p.kc_s0 = k_cache->stride[0];
+    p.kc_s1 = k_cache->stride[1];
+    p.kc_s2 = k_cache->stride[2];
+    p.vc_s0 = v_cache->stride[0];
+    p.vc_s1 = v_cache->stride[1];
+    p.vc_s2 = v_cache->stride[2];
+    ProfScope ps(PA_KERNEL_DECODE, st);
+    e = launch_decode_f32(p, st);
+  } else {
+    CUtensorMap tmK, tmV;
+    if ((r = make_cache_map(k_cache, &tmK)) || (r = make_cache_map(v_cache, &tmV))) return r;
+    ProfScope ps(PA_KERNEL_DECODE, st);
+    if (kind == KIND_BF16 || kind == KIND_F16) e = launch_decode_mma_16(p, kind, tmK, tmV, st);
+    else e = launch_decode_mma_fp8(p, kind, tmK, tmV, st);
+  }
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (max_parts > 1) {
+    ProfScope ps(PA_KERNEL_REDUCE, st);
+    e = launch_reduce(p, q->dtype, st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+PA_API int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                        const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                        const float *k_scale, const float *v_scale, int partition_size, void *workspace,
+                        size_t workspace_bytes, int *device_error, pa_stream_t stream) {
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, k_scale, v_scale,
+                     partition_size, workspace, workspace_bytes, false, device_error, stream);
+}
+
+PA_API int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                     const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                     pa_stream_t stream) {
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, nullptr, nullptr, 0,
+                     nullptr, 0, true, nullptr, stream);
+}
+
+PA_API int pa_check_device_error(int *device_error, int *bits_out, pa_stream_t stream) {
+  if (!device_error) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int bits = 0;
+  if (cudaMemcpyAsync(&bits, device_error, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(device_error, 0, sizeof(int), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  if (bits & (PA_DEVERR_SLOT_RANGE | PA_DEVERR_BLOCK_RANGE | PA_DEVERR_SEQLEN_RANGE)) return PA_ERR_DEVICE_BOUNDS;
+  if (bits & PA_DEVERR_WAIT_TIMEOUT) return PA_ERR_DEVICE_TIMEOUT;
+  return PA_OK;
+}
+
+PA_API int pa_profile_enable(int on) {
+  Profiler &P = prof();
+  std::lock_guard<std::mutex> g(P.mu);
+  P.on = on != 0;
+  return PA_OK;
+}
+
+PA_API int pa_profile_read(int kind, double *total_ms, long long *launches) {
+  if (kind < 0 || kind > 2) return PA_ERR_INVALID_ARG;
+  Profiler &P = prof();
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+  {
+    std::lock_guard<std::mutex> g(P.mu);
+    ev.swap(P.ev[kind]);
+  }
+  double ms = 0.0;
+  int rc = PA_OK;
+  for (auto &pr : ev) {
+    float t = 0.f;
+    if (cudaEventSynchronize(pr.second) != cudaSuccess || cudaEventElapsedTime(&t, pr.first, pr.second) != cudaSuccess)
+      rc = PA_ERR_CUDA;
+    ms += t;
+  }
+  {
+    std::lock_guard<std::mutex> g(P.mu);
+    for (auto &pr : ev) {
+      P.pool.push_back(pr.first);
+      P.pool.push_back(pr.second);
+    }
+  }
+  if (total_ms) *total_ms = ms;
+  if (launches) *launches = static_cast<long long>(ev.size());
+  return rc;
+}

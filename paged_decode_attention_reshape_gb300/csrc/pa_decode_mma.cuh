@@ -1,0 +1,448 @@
+// pa_decode_mma.cuh -- paged decode attention on tensor cores (bf16 / f16 / e4m3 caches).
+//
+// What it computes ("Inside vLLM CUDA Kernels", Part 3; "vLLM 源码完全拆解（七）"):
+// for each sequence s and query head h, o = sum_t softmax_t(scale * q . k_t) v_t
+// over the first seq_lens[s] tokens, reading token t of KV head h / G from
+// physical block block_table[s][t / 16], offset t % 16.
+//
+// Work unit (one CTA): sequence s, KV head g, a group of up to 8 of its query
+// heads, and one split-KV partition of pages.  All query heads of the group share
+// every K/V page the CTA loads, so each page is read from HBM once per KV head,
+// not once per query head.
+//
+// Inside a CTA, warp w takes pages w, w+W, w+2W, ... of the partition and runs its
+// own pipeline: lane 0 resolves the physical block through block_table and issues
+// two TMA tensor loads (K page, V page) into one of STAGES shared-memory stages,
+// completing on that stage's mbarrier; the warp waits on the barrier (bounded),
+// computes, and refills the stage STAGES pages ahead.  One (block, kv head)
+// page of the HND cache is 16 rows x D elements; TMA writes it with the 128-byte
+// swizzle so the tensor-core fragment loads below are bank-conflict free.
+//
+// Per 16-token page and the warp's 8-wide head group:
+//   scores  S[16 tok x 8 heads] = K_page[16 x D] . Q^T[D x 8]     (mma m16n8k16, fp32 acc)
+//   online softmax per head (log2 domain): running max m, rescale alpha, p = 2^(s-m),
+//           partial row sums kept per lane and reduced once at the end;
+//           tokens t >= seq_len get -inf (never in the max or the denominator)
+//   output  O^T[D x 8 heads] += V_page^T[D x 16 tok] . P^T[16 tok x 8 heads]
+//           with P split into hi + lo halves of the 16-bit type (two mmas), so the
+//           probabilities keep ~16 bits; V rows t >= seq_len are zeroed before the
+//           product, so stale or NaN tail values never reach the output.
+// The score fragment is turned into the P^T operand with movmatrix (transpose of
+// an 8x8 tile in registers); no shared-memory round trip.
+//
+// E4M3 caches: codes are widened to f16 exactly (cvt e4m3x2 -> f16x2) and the
+// f16 tensor-core path is used; the query is scaled by a power of two per head so
+// that its largest element lies in [2^14, 2^15) and rounded to f16 (exact for a
+// bf16 query in that range); the power of two and k_scale are folded into the
+// score scale, v_scale into the final output.  K fragments use a permuted
+// head-dimension order (each lane reads 32 contiguous bytes of a row) and the
+// query uses the same permutation, which leaves q . k unchanged.
+//
+// After the last page, each warp writes its (m, l, acc) to its own shared-memory
+// region; the CTA merges the W warp states with max/LSE rescaling and writes
+// either the normalised output (unsplit) or the partition's state to the
+// workspace for the split-KV reduce.
+#pragma once
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before a wait gives up (>= ~20 ms)
+
+template <int KIND, int D, int W, int STAGES>
+struct MmaCfg {
+  static constexpr bool FP8 = KIND == KIND_FP8_BF16Q || KIND == KIND_FP8_F16Q;
+  static constexpr bool QBF16 = KIND == KIND_BF16 || KIND == KIND_FP8_BF16Q;  // query/output bf16
+  static constexpr bool MMA_BF16 = KIND == KIND_BF16;
+  static constexpr int ELEM = FP8 ? 1 : 2;     // cache element bytes
+  static constexpr int ROWB = D * ELEM;        // bytes of one token row of a page
+  static constexpr int NBOX = ROWB / 128;      // 128-byte TMA boxes across a row
+  static constexpr int BOXE = 128 / ELEM;      // elements per box row
+  static constexpr int PAGEB = kBlock * ROWB;  // one (block, kv head) page
+  static constexpr int STAGEB = 2 * PAGEB;     // K page + V page
+  static constexpr int KT = D / 16;            // k-steps of Q.K^T = d-tiles of P.V
+  static constexpr int THREADS = W * 32;
+  static constexpr size_t SMEM = 1024 + static_cast<size_t>(W) * STAGES * STAGEB + W * STAGES * 8;
+  static_assert(ROWB % 128 == 0, "page rows must be whole 128-byte swizzle spans");
+  static_assert(STAGES * STAGEB >= 64 + 8 * D * 4, "warp region must hold the merge state");
+};
+
+template <int KIND, int D, int W, int STAGES>
+__global__ void __launch_bounds__(W * 32)
+    decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+  using C = MmaCfg<KIND, D, W, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;  // 128B-swizzle boxes need 1 KiB alignment
+  uint8_t *const sgen = smem_raw + (sbase - raw_u32);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int s = blockIdx.z, part = blockIdx.x;
+  const int g = blockIdx.y / p.HG, hg = blockIdx.y - g * p.HG;
+  const int h0 = g * p.G + hg * 8;      // first query head of this CTA
+  const int ng = min(8, p.G - hg * 8);  // query heads in the group
+  const bool split = p.max_parts > 1;
+  using OutT = typename std::conditional<C::QBF16, __nv_bfloat16, __half>::type;
+
+  const int len = __ldg(p.seq_lens + s);
+  if (len < 0 || len > p.max_blocks * kBlock) {
+    if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
+    return;
+  }
+  const int npages = (len + kBlock - 1) / kBlock;
+  const int pb = part * p.pages_per_part;
+  const int pe = min(npages, pb + p.pages_per_part);
+  if (pb >= pe) {
+    if (!split && part == 0) {  // empty sequence: zero output rows
+      for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
+        OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D;
+        *o = OutT(0.f);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- pipeline
+  const int nmine = (pe - pb > warp) ? (pe - pb - warp + W - 1) / W : 0;
+  const uint32_t stage0 = sbase + static_cast<uint32_t>(warp * STAGES * C::STAGEB);
+  const uint32_t bar0 = sbase + static_cast<uint32_t>(W * STAGES * C::STAGEB + warp * STAGES * 8);
+  if (lane == 0) {
+    for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncwarp();
+
+  const uint64_t pol = policy_evict_first();
+  const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
+  bool bad = false;
+  int pid_reg = 0;  // lane i: physical block of my page (32 * chunk + i)
+
+  auto issue = [&](int kk) {  // whole warp; kk increases by one per call
+    if ((kk & 31) == 0) {
+      const int k2 = kk + lane;
+      pid_reg = (k2 < nmine) ? __ldg(bt + pb + warp + k2 * W) : 0;
+    }
+    int pid = __shfl_sync(0xffffffffu, pid_reg, kk & 31);
+    if (pid < 0 || pid >= p.num_blocks) {
+      bad = true;
+      if (lane == 0 && p.err) atomicOr(p.err, kErrBlock);
+      pid = 0;  // load a valid block; the CTA writes nothing
+    }
+    if (lane == 0) {
+      const int st = kk % STAGES;
+      const uint32_t bar = bar0 + 8 * st;
+      const uint32_t kdst = stage0 + st * C::STAGEB;
+      mbar_arrive_expect_tx(bar, C::STAGEB);
+#pragma unroll
+      for (int b = 0; b < C::NBOX; ++b) tma_load_4d(kdst + b * 2048, &tmK, bar, b * C::BOXE, 0, g, pid, pol);
+#pragma unroll
+      for (int b = 0; b < C::NBOX; ++b)
+        tma_load_4d(kdst + C::PAGEB + b * 2048, &tmV, bar, b * C::BOXE, 0, g, pid, pol);
+    }
+  };
+
+  const int npre = min(STAGES, nmine);
+  for (int kk = 0; kk < npre; ++kk) issue(kk);
+
+  // ------------------------------------------------------- query fragments
+  const int qh = lane >> 2, qc = lane & 3;  // fragment row (head / token) and column group
+  const bool qvalid = qh < ng;
+  const char *qrow = static_cast<const char *>(p.q) +
+                     (static_cast<int64_t>(s) * p.q_ss + static_cast<int64_t>(h0 + (qvalid ? qh : 0)) * p.q_hs) * 2;
+  uint32_t qf[C::KT][2];
+  float sc0, sc1;  // score scale (log2 units) of this lane's two head columns 2qc, 2qc+1
+  if constexpr (!C::FP8) {
+#pragma unroll
+    for (int j = 0; j < C::KT; ++j) {
+      const uint32_t lo = __ldg(reinterpret_cast<const uint32_t *>(qrow + (16 * j + 2 * qc) * 2));
+      const uint32_t hi = __ldg(reinterpret_cast<const uint32_t *>(qrow + (16 * j + 8 + 2 * qc) * 2));
+      qf[j][0] = qvalid ? lo : 0u;
+      qf[j][1] = qvalid ? hi : 0u;
+    }
+    sc0 = sc1 = p.scale_log2;
+  } else {
+    // lane covers d = 128 b + 32 qc + [0, 32) of head qh, box b
+    uint4 raw[C::NBOX][4];
+    float mx = 0.f;
+#pragma unroll
+    for (int b = 0; b < C::NBOX; ++b) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        raw[b][i] = __ldg(reinterpret_cast<const uint4 *>(qrow + (128 * b + 32 * qc + 8 * i) * 2));
+        const uint32_t w4[4] = {raw[b][i].x, raw[b][i].y, raw[b][i].z, raw[b][i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = C::QBF16 ? unpack_bf16(w4[e]) : unpack_f16(w4[e]);
+          mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    int ex = 0;
+    if (mx > 0.f && mx <= 3.0e38f) {
+      frexpf(mx, &ex);  // mx = f * 2^ex, f in [0.5, 1)
+      ex -= 1;          // floor(log2 mx)
+    }
+    const int sh = max(-120, min(120, 14 - ex));
+    const float sfac = ldexpf(1.f, sh);  // max |q| * sfac in [2^14, 2^15)
+#pragma unroll
+    for (int b = 0; b < C::NBOX; ++b) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w4[4] = {raw[b][i].x, raw[b][i].y, raw[b][i].z, raw[b][i].w};
+        // elements 8i .. 8i+7 of the lane's 32 = k-steps j = 2i, 2i+1 (4 elements each)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const float2 f0 = C::QBF16 ? unpack_bf16(w4[2 * jj]) : unpack_f16(w4[2 * jj]);
+          const float2 f1 = C::QBF16 ? unpack_bf16(w4[2 * jj + 1]) : unpack_f16(w4[2 * jj + 1]);
+          const int j = b * 8 + 2 * i + jj;
+          qf[j][0] = qvalid ? pack_f16(f0.x * sfac, f0.y * sfac) : 0u;
+          qf[j][1] = qvalid ? pack_f16(f1.x * sfac, f1.y * sfac) : 0u;
+        }
+      }
+    }
+    const float ks = p.k_scale ? __ldg(p.k_scale) : 1.f;
+    const float sf0 = __shfl_sync(0xffffffffu, sfac, (2 * qc) * 4);
+    const float sf1 = __shfl_sync(0xffffffffu, sfac, (2 * qc + 1) * 4);
+    sc0 = p.scale_log2 * ks / sf0;
+    sc1 = p.scale_log2 * ks / sf1;
+  }
+
+  // --------------------------------------------------------------- main loop
+  float acc[C::KT][4];
+#pragma unroll
+  for (int t = 0; t < C::KT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int ra = lane >> 2;  // token row of score fragments (and +8)
+
+  for (int k = 0; k < nmine; ++k) {
+    const int st = k % STAGES;
+    if (!mbar_wait_bounded(bar0 + 8 * st, (k / STAGES) & 1, kWaitLimit)) {
+      bad = true;
+      if (lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
+      for (int k2 = k + 1; k2 < min(nmine, k + STAGES); ++k2)  // drain copies in flight
+        mbar_wait_bounded(bar0 + 8 * (k2 % STAGES), (k2 / STAGES) & 1, kWaitLimit);
+      break;
+    }
+    const uint32_t kb = stage0 + st * C::STAGEB;
+    const uint32_t vb = kb + C::PAGEB;
+    const int page = pb + warp + k * W;
+    const int nv = min(kBlock, len - page * kBlock);  // valid tokens in this page
+
+    // ---- scores: two accumulation chains over the k-steps
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!C::FP8) {
+      const int lrow = (lane & 7) | (lane & 8);
+      const int lhi = lane >> 4;
+#pragma unroll
+      for (int j = 0; j < C::KT; ++j) {
+        const int chunk = ((j & 3) << 1) | lhi;
+        uint32_t a[4];
+        ldmatrix_x4(a, kb + (j >> 2) * 2048 + lrow * 128 + ((chunk ^ (lrow & 7)) << 4));
+        if constexpr (C::MMA_BF16) {
+          if (j & 1) mma_bf16(c1, a, qf[j][0], qf[j][1]); else mma_bf16(c0, a, qf[j][0], qf[j][1]);
+        } else {
+          if (j & 1) mma_f16(c1, a, qf[j][0], qf[j][1]); else mma_f16(c0, a, qf[j][0], qf[j][1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int b = 0; b < C::NBOX; ++b) {
+        const uint32_t rowa = kb + b * 2048 + ra * 128, rowb = rowa + 8 * 128;
+        const uint32_t ch0 = static_cast<uint32_t>(((2 * qc) ^ ra) << 4);
+        const uint32_t ch1 = static_cast<uint32_t>(((2 * qc + 1) ^ ra) << 4);
+        const uint4 A0 = lds128(rowa + ch0), A1 = lds128(rowa + ch1);
+        const uint4 B0 = lds128(rowb + ch0), B1 = lds128(rowb + ch1);
+        const uint32_t wa[8] = {A0.x, A0.y, A0.z, A0.w, A1.x, A1.y, A1.z, A1.w};
+        const uint32_t wb[8] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t a[4];
+          a[0] = e4m3x2_to_f16x2(wa[j]);        // row ra,   d 4j, 4j+1
+          a[1] = e4m3x2_to_f16x2(wb[j]);        // row ra+8
+          a[2] = e4m3x2_to_f16x2(wa[j] >> 16);  // row ra,   d 4j+2, 4j+3
+          a[3] = e4m3x2_to_f16x2(wb[j] >> 16);  // row ra+8
+          if (j & 1) mma_f16(c1, a, qf[b * 8 + j][0], qf[b * 8 + j][1]);
+          else mma_f16(c0, a, qf[b * 8 + j][0], qf[b * 8 + j][1]);
+        }
+      }
+    }
+
+    // ---- online softmax (fragment: rows ra, ra+8 = tokens; columns 2qc, 2qc+1 = heads)
+    const bool va = ra < nv, vb8 = ra + 8 < nv;
+    const float s0 = va ? (c0[0] + c1[0]) * sc0 : -INFINITY;
+    const float s1 = va ? (c0[1] + c1[1]) * sc1 : -INFINITY;
+    const float s2 = vb8 ? (c0[2] + c1[2]) * sc0 : -INFINITY;
+    const float s3 = vb8 ? (c0[3] + c1[3]) * sc1 : -INFINITY;
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // 0 on the first page (m = -inf)
+    const float p0 = ex2(s0 - mn0), p1 = ex2(s1 - mn1), p2 = ex2(s2 - mn0), p3 = ex2(s3 - mn1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int t = 0; t < C::KT; ++t) {
+      acc[t][0] *= al0;
+      acc[t][1] *= al1;
+      acc[t][2] *= al0;
+      acc[t][3] *= al1;
+    }
+
+    // ---- P^T operand: hi + lo 16-bit halves, transposed in registers
+    uint32_t bh0, bh1, bl0, bl1;
+    if constexpr (C::MMA_BF16) {
+      const uint32_t ha = pack_bf16(p0, p1), hb = pack_bf16(p2, p3);
+      const float2 fa = unpack_bf16(ha), fb = unpack_bf16(hb);
+      bh0 = movmatrix_trans(ha);
+      bh1 = movmatrix_trans(hb);
+      bl0 = movmatrix_trans(pack_bf16(p0 - fa.x, p1 - fa.y));
+      bl1 = movmatrix_trans(pack_bf16(p2 - fb.x, p3 - fb.y));
+    } else {
+      const uint32_t ha = pack_f16(p0, p1), hb = pack_f16(p2, p3);
+      const float2 fa = unpack_f16(ha), fb = unpack_f16(hb);
+      bh0 = movmatrix_trans(ha);
+      bh1 = movmatrix_trans(hb);
+      bl0 = movmatrix_trans(pack_f16(p0 - fa.x, p1 - fa.y));
+      bl1 = movmatrix_trans(pack_f16(p2 - fb.x, p3 - fb.y));
+    }
+
+    // ---- O^T += V^T . P^T (tail rows of the last page zeroed first)
+    if constexpr (!C::FP8) {
+      const uint32_t mA = (2 * qc < nv ? 0x0000FFFFu : 0u) | (2 * qc + 1 < nv ? 0xFFFF0000u : 0u);
+      const uint32_t mB = (2 * qc + 8 < nv ? 0x0000FFFFu : 0u) | (2 * qc + 9 < nv ? 0xFFFF0000u : 0u);
+      const int vtok = (lane & 7) | ((lane >> 4) << 3);
+      const int vhalf = (lane >> 3) & 1;
+#pragma unroll
+      for (int t = 0; t < C::KT; ++t) {
+        const int cidx = 2 * t + vhalf;  // 16-byte chunk of the row
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vb + (cidx >> 3) * 2048 + vtok * 128 + (((cidx & 7) ^ (vtok & 7)) << 4));
+        if (nv < kBlock) {
+          a[0] &= mA;
+          a[1] &= mA;
+          a[2] &= mB;
+          a[3] &= mB;
+        }
+        if constexpr (C::MMA_BF16) {
+          mma_bf16(acc[t], a, bh0, bh1);
+          mma_bf16(acc[t], a, bl0, bl1);
+        } else {
+          mma_f16(acc[t], a, bh0, bh1);
+          mma_f16(acc[t], a, bl0, bl1);
+        }
+      }
+    } else {
+      const int t0 = 2 * qc, t1 = 2 * qc + 1, t2 = 2 * qc + 8, t3 = 2 * qc + 9;
+#pragma unroll
+      for (int b = 0; b < C::NBOX; ++b) {
+        const uint32_t pgb = vb + b * 2048;
+        uint4 w0 = lds128(pgb + t0 * 128 + ((ra ^ (t0 & 7)) << 4));
+        uint4 w1 = lds128(pgb + t1 * 128 + ((ra ^ (t1 & 7)) << 4));
+        uint4 w2 = lds128(pgb + t2 * 128 + ((ra ^ (t2 & 7)) << 4));
+        uint4 w3 = lds128(pgb + t3 * 128 + ((ra ^ (t3 & 7)) << 4));
+        if (nv < kBlock) {
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          if (t0 >= nv) w0 = z;
+          if (t1 >= nv) w1 = z;
+          if (t2 >= nv) w2 = z;
+          if (t3 >= nv) w3 = z;
+        }
+        const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
+        const uint32_t x2[4] = {w2.x, w2.y, w2.z, w2.w}, x3[4] = {w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          // d0 = 128b + 16ra + 2t (fragment row ra), d1 = d0 + 1 (row ra + 8)
+          const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
+          const uint32_t p01 = __byte_perm(x0[t >> 1], x1[t >> 1], sel);
+          const uint32_t p23 = __byte_perm(x2[t >> 1], x3[t >> 1], sel);
+          uint32_t a[4];
+          a[0] = e4m3x2_to_f16x2(p01);        // d0, tokens t0 t1
+          a[1] = e4m3x2_to_f16x2(p01 >> 16);  // d1, tokens t0 t1
+          a[2] = e4m3x2_to_f16x2(p23);        // d0, tokens t2 t3
+          a[3] = e4m3x2_to_f16x2(p23 >> 16);  // d1, tokens t2 t3
+          mma_f16(acc[b * 8 + t], a, bh0, bh1);
+          mma_f16(acc[b * 8 + t], a, bl0, bl1);
+        }
+      }
+    }
+
+    __syncwarp();
+    if (k + STAGES < nmine) {
+      fence_proxy_async_smem();
+      issue(k + STAGES);
+    }
+  }
+
+  // ------------------------------------------------------ merge warp states
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  // warp region (its own stage buffers, no copies in flight): ml[8][2], then acc[8][D]
+  float *wml = reinterpret_cast<float *>(sgen + warp * STAGES * C::STAGEB);
+  float *wacc = wml + 16;
+  if (ra == 0) {
+    wml[2 * (2 * qc)] = m0;
+    wml[2 * (2 * qc) + 1] = l0;
+    wml[2 * (2 * qc + 1)] = m1;
+    wml[2 * (2 * qc + 1) + 1] = l1;
+  }
+#pragma unroll
+  for (int t = 0; t < C::KT; ++t) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int head = 2 * qc + (i & 1);
+      int d;
+      if constexpr (!C::FP8) d = 16 * t + ra + 8 * (i >> 1);
+      else d = 128 * (t >> 3) + 16 * ra + 2 * (t & 7) + (i >> 1);
+      wacc[head * D + d] = acc[t][i];
+    }
+  }
+  const bool any_bad = __syncthreads_or(bad);
+  if (any_bad) return;
+
+  const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.f;
+  for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
+    const int hh = i / D, d = i - hh * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
+      M = fmaxf(M, ml[2 * hh]);
+    }
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
+      const float mw = ml[2 * hh];
+      const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      den += sc * ml[2 * hh + 1];
+      num += sc * ml[16 + hh * D + d];
+    }
+    const int h = h0 + hh;
+    if (!split) {
+      OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h) * p.out_hs + d;
+      *o = OutT(den > 0.f ? num / den * vs : 0.f);
+    } else {
+      const int64_t row = (static_cast<int64_t>(s) * p.Hq + h) * p.max_parts + part;
+      p.part_acc[row * D + d] = num;
+      if (d == 0) p.part_ml[row] = make_float2(M, den);
+    }
+  }
+}
+
+}  // namespace pa

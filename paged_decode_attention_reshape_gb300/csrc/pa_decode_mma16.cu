@@ -1,0 +1,40 @@
+// pa_decode_mma16.cu -- instantiations of the tensor-core decode kernel for
+// bf16 and f16 caches (see pa_decode_mma.cuh).
+#include "pa_decode_mma.cuh"
+
+namespace pa {
+namespace {
+
+template <int KIND, int D>
+cudaError_t go(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
+  constexpr int W = mma_warps(KIND, D), ST = mma_stages(KIND, D);
+  using C = MmaCfg<KIND, D, W, ST>;
+  static_assert(C::SMEM == mma_smem(KIND, D), "shape table out of sync");
+  auto kern = decode_mma_kernel<KIND, D, W, ST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.max_parts, p.Hkv * p.HG, p.S);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(p, tmK, tmV);
+  return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t by_d(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
+  switch (p.D) {
+    case 64: return go<KIND, 64>(p, tmK, tmV, st);
+    case 128: return go<KIND, 128>(p, tmK, tmV, st);
+    case 256: return go<KIND, 256>(p, tmK, tmV, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma_16(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                 cudaStream_t st) {
+  if (kind == KIND_BF16) return by_d<KIND_BF16>(p, tmK, tmV, st);
+  if (kind == KIND_F16) return by_d<KIND_F16>(p, tmK, tmV, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

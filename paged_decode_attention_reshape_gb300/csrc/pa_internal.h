@@ -1,0 +1,84 @@
+// pa_internal.h -- launch parameters shared by the host API and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr int kBlock = PA_BLOCK_SIZE;  // tokens per KV-cache block (one "page")
+
+// Cache element kinds of the decode kernels (query/output type in brackets).
+enum DecodeKind : int {
+  KIND_BF16 = 0,      // bf16 cache [bf16 q]
+  KIND_F16 = 1,       // f16 cache [f16 q]
+  KIND_FP8_BF16Q = 2, // e4m3 cache [bf16 q]
+  KIND_FP8_F16Q = 3,  // e4m3 cache [f16 q]
+  KIND_F32 = 4        // fp32 cache [fp32 q], CUDA-core path
+};
+
+struct WriteParams {
+  const void *key, *value;
+  void *k_cache, *v_cache;
+  const int64_t *slot_mapping;
+  int64_t T;
+  int Hkv, D;
+  int64_t key_ts, key_hs, val_ts, val_hs;          // elements
+  int64_t kc_s0, kc_s1, kc_s2, vc_s0, vc_s1, vc_s2; // elements
+  int64_t num_slots;                                // num_blocks * 16
+  const float *k_scale, *v_scale;                   // nullable
+  int *err;                                         // nullable
+};
+
+struct DecodeParams {
+  void *out;
+  const void *q;
+  int64_t out_ss, out_hs, q_ss, q_hs;  // elements
+  const int32_t *block_table;
+  int64_t bt_ss;
+  const int32_t *seq_lens;
+  int S, Hq, Hkv, G, HG, D;            // HG = head groups of <= 8 query heads per KV head
+  int num_blocks, max_blocks;
+  float scale_log2;                    // softmax scale * log2(e)
+  const float *k_scale, *v_scale;      // nullable (1.0)
+  int pages_per_part;                  // partition length in pages
+  int max_parts;                       // partitions of the longest sequence (1 = unsplit)
+  float2 *part_ml;                     // [S, Hq, max_parts] (m in log2 units, l)
+  float *part_acc;                     // [S, Hq, max_parts, D]
+  int *err;                            // nullable
+  // fp32 path only: direct cache pointers and strides (elements)
+  const float *kc, *vc;
+  int64_t kc_s0, kc_s1, kc_s2, vc_s0, vc_s1, vc_s2;
+};
+
+// Error bits (mirror PA_DEVERR_* of pa.h).
+constexpr int kErrSlot = PA_DEVERR_SLOT_RANGE;
+constexpr int kErrBlock = PA_DEVERR_BLOCK_RANGE;
+constexpr int kErrSeqLen = PA_DEVERR_SEQLEN_RANGE;
+constexpr int kErrTimeout = PA_DEVERR_WAIT_TIMEOUT;
+
+// Launchers (defined next to their kernels).  Return a cudaError_t.
+cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, int sm_count, cudaStream_t st);
+
+// Tensor-core kernel shape per (kind, head size): warps per CTA and pipeline
+// stages per warp.  Shared memory = W * STAGES * 2 pages (+ alignment, barriers).
+constexpr int mma_warps(int kind, int D) { return (void)kind, (void)D, 4; }
+constexpr int mma_stages(int kind, int D) {
+  return (kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) ? (D <= 128 ? 4 : 3) : (D <= 64 ? 4 : D <= 128 ? 3 : 2);
+}
+constexpr size_t mma_smem(int kind, int D) {
+  return 1024 + static_cast<size_t>(mma_warps(kind, D)) * mma_stages(kind, D) *
+                    (2 * kBlock * D * ((kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) ? 1 : 2) + 8);
+}
+
+cudaError_t launch_decode_mma_16(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                 cudaStream_t st);  // KIND_BF16, KIND_F16
+cudaError_t launch_decode_mma_fp8(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                  cudaStream_t st);  // KIND_FP8_*
+cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st);
+cudaError_t launch_reduce(const DecodeParams &p, int out_dtype, cudaStream_t st);
+
+}  // namespace pa

@@ -1,0 +1,137 @@
+// pa_write.cu -- the paged KV-cache write (slot_mapping scatter).
+//
+// Follows "Inside vLLM CUDA Kernels: KV-Cache Writes and Paged Attention",
+// Part 2: each new token has one destination slot; slot < 0 means padding with
+// no destination; slot -> (block = slot / 16, offset = slot % 16); the element
+// conversion is a copy, or scale-and-convert for an FP8 cache.
+//
+// GB300 design: the work item is one 16-byte pack of one (token, kv head) row,
+// for K and V together.  Adjacent threads take adjacent packs of the source
+// (fully coalesced reads), and each destination (block, head, offset) row is a
+// contiguous run of D * elem bytes in the HND cache, so a warp's stores cover
+// whole 32-byte sectors.  Sources are read once with no L1 allocation.  The grid
+// is a multiple of the SM count, grid-striding over all packs.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__device__ __forceinline__ uint4 ld_once(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Element type codes for the template (match pa_dtype values).
+template <int DT> struct In;
+template <> struct In<PA_F32> { static constexpr int bytes = 4; };
+template <> struct In<PA_BF16> { static constexpr int bytes = 2; };
+template <> struct In<PA_F16> { static constexpr int bytes = 2; };
+
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&x)[16 / In<DT>::bytes]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (DT == PA_F32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = __uint_as_float(w[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = (DT == PA_BF16) ? unpack_bf16(w[i]) : unpack_f16(w[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  }
+}
+
+// E4M3 code pair of (a / s, b / s): IEEE division rounded to nearest, then
+// round-to-nearest-even with saturation (cvt ... satfinite); low byte = a.
+__device__ __forceinline__ uint32_t quant2(float a, float b, float s) {
+  const float2 y = make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3));
+}
+
+template <int DT>
+__device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, float s) {
+  constexpr int E = 16 / In<DT>::bytes;
+  float x[E];
+  unpack8<DT>(v, x);
+  if constexpr (E == 8) {
+    uint2 o;
+    o.x = quant2(x[0], x[1], s) | (quant2(x[2], x[3], s) << 16);
+    o.y = quant2(x[4], x[5], s) | (quant2(x[6], x[7], s) << 16);
+    *reinterpret_cast<uint2 *>(dst) = o;
+  } else {
+    *reinterpret_cast<uint32_t *>(dst) = quant2(x[0], x[1], s) | (quant2(x[2], x[3], s) << 16);
+  }
+}
+
+template <int DT, bool FP8>
+__global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
+  constexpr int IB = In<DT>::bytes;
+  constexpr int EPP = 16 / IB;            // elements per 16-byte pack
+  constexpr int CB = FP8 ? 1 : IB;        // cache element bytes
+  const int ppr = p.D / EPP;              // packs per (token, head) row
+  const int64_t per_tok = static_cast<int64_t>(p.Hkv) * ppr;
+  const int64_t total = p.T * per_tok;
+  float ks = 1.f, vs = 1.f;
+  if (FP8) {
+    if (p.k_scale) ks = __ldg(p.k_scale);
+    if (p.v_scale) vs = __ldg(p.v_scale);
+  }
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / per_tok;
+    const int r = static_cast<int>(i - t * per_tok);
+    const int h = r / ppr;
+    const int64_t e = static_cast<int64_t>(r - h * ppr) * EPP;
+    const int64_t slot = __ldg(p.slot_mapping + t);
+    if (slot < 0) continue;  // padding row: no destination
+    if (slot >= p.num_slots) {
+      if (p.err) atomicOr(p.err, kErrSlot);
+      continue;
+    }
+    const int64_t blk = slot / kBlock, off = slot % kBlock;
+    const uint4 kv = ld_once(static_cast<const char *>(p.key) + (t * p.key_ts + h * p.key_hs + e) * IB);
+    const uint4 vv = ld_once(static_cast<const char *>(p.value) + (t * p.val_ts + h * p.val_hs + e) * IB);
+    char *kd = static_cast<char *>(p.k_cache) + (blk * p.kc_s0 + h * p.kc_s1 + off * p.kc_s2 + e) * CB;
+    char *vd = static_cast<char *>(p.v_cache) + (blk * p.vc_s0 + h * p.vc_s1 + off * p.vc_s2 + e) * CB;
+    if constexpr (!FP8) {
+      *reinterpret_cast<uint4 *>(kd) = kv;
+      *reinterpret_cast<uint4 *>(vd) = vv;
+    } else {
+      store_fp8<DT>(kd, kv, ks);
+      store_fp8<DT>(vd, vv, vs);
+    }
+  }
+}
+
+template <int DT, bool FP8>
+cudaError_t launch_one(const WriteParams &p, int sm_count, cudaStream_t st) {
+  constexpr int EPP = 16 / In<DT>::bytes;
+  const int64_t total = p.T * p.Hkv * (p.D / EPP);
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;  // 8 x 256 threads per SM, grid-stride
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  write_kernel<DT, FP8><<<static_cast<unsigned>(blocks), threads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, int sm_count, cudaStream_t st) {
+  const bool fp8 = cache_dtype == PA_FP8_E4M3;
+  switch (in_dtype) {
+    case PA_F32: return fp8 ? launch_one<PA_F32, true>(p, sm_count, st) : launch_one<PA_F32, false>(p, sm_count, st);
+    case PA_BF16: return fp8 ? launch_one<PA_BF16, true>(p, sm_count, st) : launch_one<PA_BF16, false>(p, sm_count, st);
+    case PA_F16: return fp8 ? launch_one<PA_F16, true>(p, sm_count, st) : launch_one<PA_F16, false>(p, sm_count, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa
