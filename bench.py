@@ -112,8 +112,8 @@ def workspace_for(st: Staged, partition_size: int):
     w = st.w
     code = {"f32": pa.PA_F32, "bf16": pa.PA_BF16, "e4m3": pa.PA_FP8_E4M3}[w.cache_dtype]
     P, nparts = pa.pa_decode_plan(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, code, 0, partition_size)
-    nbytes = pa.pa_decode_workspace_size(w.S, w.Hq, w.D, w.max_blocks, P) if P > 0 else 0
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=st.q.device)
+    nbytes = pa.pa_decode_workspace_size(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, P) if P > 0 else 0
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=st.q.device)   # zero before first use
     return P, nparts, ws
 
 
@@ -241,19 +241,20 @@ def time_steps(st, K, flush, partition_size, ws, profile=False):
     if profile:
         pa.pa_profile_read(pa.PA_KERNEL_WRITE)
         pa.pa_profile_read(pa.PA_KERNEL_DECODE)
-        pa.pa_profile_read(pa.PA_KERNEL_REDUCE)
         pa.pa_profile_enable(True)
     torch.cuda.synchronize()
     for i in range(K):
         flush.zero_()
         ev[i][0].record()
+        torch.cuda.nvtx.range_push("step")
         run_step(st, partition_size, ws)
+        torch.cuda.nvtx.range_pop()
         ev[i][1].record()
     torch.cuda.synchronize()
     prof = None
     if profile:
         pa.pa_profile_enable(False)
-        prof = {k: pa.pa_profile_read(k) for k in (pa.PA_KERNEL_WRITE, pa.PA_KERNEL_DECODE, pa.PA_KERNEL_REDUCE)}
+        prof = {k: pa.pa_profile_read(k) for k in (pa.PA_KERNEL_WRITE, pa.PA_KERNEL_DECODE)}
     return [a.elapsed_time(b) for a, b in ev], prof
 
 
@@ -408,7 +409,8 @@ def main(argv=None):
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--quick", action="store_true", help="setup + a few steps only (profiling runs)")
+    ap.add_argument("--quick", action="store_true", help="setup + warm-up steps only (profiling runs)")
+    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the timed steps")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return main_reference(args)
@@ -439,7 +441,7 @@ def main(argv=None):
         sampler.start()
         time.sleep(0.5)
         # soak: keep the GPU busy ~1 s so the sampled clocks are the loaded ones
-        t_end = time.time() + 1.0
+        t_end = time.time() + (0.0 if args.no_soak else 1.0)
         while time.time() < t_end:
             for _ in range(20):
                 flush.zero_()
@@ -464,11 +466,10 @@ def main(argv=None):
     value = ws * dec_bytes / (ms * 1e-3) / 1e9
     wr_ms, wr_n = prof[pa.PA_KERNEL_WRITE]
     dk_ms, dk_n = prof[pa.PA_KERNEL_DECODE]
-    rd_ms, rd_n = prof[pa.PA_KERNEL_REDUCE]
     dk_avg = dk_ms / max(1, dk_n)
     peak, peak_src = _peaks()
     achieved = dec_bytes / (dk_avg * 1e-3) / 1e9
-    launches = wr_n + dk_n + rd_n
+    launches = wr_n + dk_n
 
     e2e = None
     if not args.no_e2e:
@@ -491,7 +492,6 @@ def main(argv=None):
         "pct_of_hbm_peak": 100.0 * value / peak,
         "tokens_per_s": ws * w.S / (ms * 1e-3),
         "decode_kernel_us": dk_avg * 1e3,
-        "reduce_kernel_us": rd_ms / max(1, rd_n) * 1e3 if rd_n else 0.0,
         "cache_write": {"GB/s": w.write_bytes() / ((wr_ms / max(1, wr_n)) * 1e-3) / 1e9,
                         "kernel_us": wr_ms / max(1, wr_n) * 1e3, "bytes": w.write_bytes()},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

@@ -137,15 +137,16 @@ int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa_tensor
  *   k_cache,      [num_blocks, Hkv, 16, D]; element type == q's, or PA_FP8_E4M3
  *   v_cache       with a PA_BF16 / PA_F16 query.
  *   block_table   PA_I32 [S, max_blocks_per_seq], innermost stride 1.  Only the
- *                 first ceil(seq_lens[s] / 16) entries of row s are read.
+ *                 first ceil(seq_lens[s] / 16) entries of row s are used; the
+ *                 rest may hold any value (padding).
  *   seq_lens      PA_I32 [S]: visible KV length of each sequence, counting the
  *                 token written in this step.  0 gives an all-zero output row.
  *   scale         softmax scale (usually 1 / sqrt(D)).
  *   num_kv_heads  Hkv; must equal k_cache->shape[1] and divide Hq.
  * Head sizes built: 64, 128, 256 (FP8 caches: 128, 256).
  * Uses a library-held workspace on the current device (grown on demand with
- * cudaMallocAsync on `stream`); calls that use it on different streams must not
- * overlap.  FP8 scales are 1.0 here; use pa_decode_ex for scales, a caller-owned
+ * cudaMallocAsync and zero-filled on `stream`); calls that use it on different
+ * streams must not overlap.  FP8 scales are 1.0 here; use pa_decode_ex for scales, a caller-owned
  * workspace, an explicit partition size or a device error word.
  */
 int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
@@ -160,11 +161,20 @@ int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, cons
  *   partition_size    KV tokens per split-KV partition: 0 = chosen by the
  *                     library's measured heuristic (pa_decode_plan), -1 = never
  *                     split, > 0 = that many tokens (rounded up to a multiple of 16).
- *   workspace,        device memory for split-KV partial states; at least
+ *   workspace,        device memory for split-KV partition states; at least
  *   workspace_bytes   pa_decode_workspace_size(...) bytes for the partition size
  *                     the call ends up using (0 bytes when it does not split).
  *                     NULL with workspace_bytes == 0 is fine for the unsplit path.
+ *                     Zero-fill it once before its first use: it holds per-unit
+ *                     arrival counters that every call leaves at zero again.  The
+ *                     library owns its contents between calls, and calls that
+ *                     share one workspace must not run concurrently.
  *   device_error      device int to OR error bits into, or NULL.
+ * Split-KV runs in the one decode launch: each partition's CTA stores its
+ * (max, exp-sum, partial output) state and the last CTA of a (sequence, kv head)
+ * unit merges them with log-sum-exp rescaling.  The decode kernel is launched as a
+ * programmatic dependent of the preceding work on `stream` and waits for it before
+ * reading any input.
  */
 int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                  const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
@@ -185,10 +195,11 @@ int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
 
 /*
  * pa_decode_workspace_size -- bytes of split-KV workspace for `partition_size`
- * tokens per partition (0 or -1 = unsplit -> 0 bytes).  Host-only.
+ * tokens per partition (0 or -1 = unsplit -> 0 bytes; invalid arguments -> 0).
+ * Host-only.
  */
-size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_size, int max_blocks_per_seq,
-                                int partition_size);
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                int max_blocks_per_seq, int partition_size);
 
 /*
  * pa_check_device_error -- synchronise `stream`, read the device error word,
@@ -206,12 +217,10 @@ const char *pa_status_string(int status);
  * pair of CUDA events recorded on its launch stream.  pa_profile_read
  * synchronises on the recorded events, returns the summed device time (ms) and
  * the launch count for one kernel kind since the last read, and clears them.
- *   kind: 0 = cache write, 1 = decode (the attention kernel itself),
- *         2 = split-KV reduce.
+ *   kind: 0 = cache write, 1 = decode (attention with the fused split-KV merge).
  */
 #define PA_KERNEL_WRITE 0
 #define PA_KERNEL_DECODE 1
-#define PA_KERNEL_REDUCE 2
 int pa_profile_enable(int on);
 int pa_profile_read(int kind, double *total_ms, long long *launches);
 

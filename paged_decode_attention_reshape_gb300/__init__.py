@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libpa_gb300.so")
 
 PA_F32, PA_BF16, PA_F16, PA_FP8_E4M3, PA_I32, PA_I64 = range(6)
 PA_KV_AUTO, PA_KV_FP8_E4M3 = 0, 1
-PA_KERNEL_WRITE, PA_KERNEL_DECODE, PA_KERNEL_REDUCE = 0, 1, 2
+PA_KERNEL_WRITE, PA_KERNEL_DECODE = 0, 1
 PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_SEQLEN_RANGE, PA_DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
 STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED_DTYPE", -3: "PA_ERR_ALIGNMENT",
           -4: "PA_ERR_WORKSPACE", -5: "PA_ERR_CUDA", -6: "PA_ERR_DEVICE_BOUNDS", -7: "PA_ERR_UNSUPPORTED_SHAPE",
@@ -77,7 +77,7 @@ def lib() -> ctypes.CDLL:
             L.pa_decode_plan.restype = i32
             L.pa_decode_plan.argtypes = [i32] * 8 + [ctypes.POINTER(i32), ctypes.POINTER(i32)]
             L.pa_decode_workspace_size.restype = ctypes.c_size_t
-            L.pa_decode_workspace_size.argtypes = [i32] * 5
+            L.pa_decode_workspace_size.argtypes = [i32] * 6
             L.pa_check_device_error.restype = i32
             L.pa_check_device_error.argtypes = [P, ctypes.POINTER(i32), P]
             L.pa_status_string.restype = ctypes.c_char_p
@@ -149,7 +149,7 @@ def pa_decode_ex(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, 
                  k_scale=None, v_scale=None, partition_size: int = 0, workspace=None, device_error=None,
                  stream=None) -> None:
     """pa_decode with FP8 scales, explicit partition size (0 heuristic, -1 unsplit), caller workspace
-    (a uint8 CUDA tensor) and device error word (int32 CUDA tensor)."""
+    (a zero-filled uint8 CUDA tensor, see pa_decode_workspace_size) and device error word (int32)."""
     args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(block_table), desc(seq_lens))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib().pa_decode_ex(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), _ptr(k_scale),
@@ -168,8 +168,10 @@ def pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_
     return P.value, n.value
 
 
-def pa_decode_workspace_size(num_seqs, num_heads, head_size, max_blocks_per_seq, partition_size) -> int:
-    return int(lib().pa_decode_workspace_size(num_seqs, num_heads, head_size, max_blocks_per_seq, partition_size))
+def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, partition_size) -> int:
+    """Bytes of split-KV workspace; zero-fill it once before first use (torch.zeros)."""
+    return int(lib().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq,
+                                              partition_size))
 
 
 def pa_check_device_error(device_error, stream=None):
@@ -188,7 +190,7 @@ def pa_profile_enable(on: bool = True) -> None:
 
 
 def pa_profile_read(kind: int):
-    """(total device ms, launches) for kind PA_KERNEL_WRITE / _DECODE / _REDUCE since the last read."""
+    """(total device ms, launches) for kind PA_KERNEL_WRITE / PA_KERNEL_DECODE since the last read."""
     ms, n = ctypes.c_double(0), ctypes.c_longlong(0)
     _check(lib().pa_profile_read(int(kind), ctypes.byref(ms), ctypes.byref(n)), "pa_profile_read")
     return ms.value, n.value

@@ -54,7 +54,7 @@ int device_sm_count() {
 struct Profiler {
   std::mutex mu;
   bool on = false;
-  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[3];
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[2];
   std::vector<cudaEvent_t> pool;
   cudaEvent_t get() {
     if (!pool.empty()) {
@@ -154,11 +154,16 @@ int ctas_per_sm(int kind, int D) {
   return std::max(1, std::min(n, 16));
 }
 
-// Partition size in tokens (0 = unsplit).  Without reading seq_lens (no host
-// sync), the plan sizes partitions from the block-table width: split only when
-// the (sequence, kv head, head group) units alone cannot fill the GPU, and
-// then cut the longest possible sequence into enough partitions for about four
-// resident waves, never below 256 tokens per partition.
+// Partition size in tokens (0 = unsplit).  The plan cannot read seq_lens (no
+// host sync), so it assumes lengths spread up to the block-table width (average
+// about half of it) and cuts that work into partitions of equal length so that
+// the GPU's resident CTA slots see about four waves.  A partition is never
+// shorter than 64 pages (1024 tokens), and when the partition would be at least
+// half the table width the call does not split at all: below those points the
+// per-CTA prologue and the partition merge cost more than the balance gains
+// (measured on GB300 over partition sizes 256..4096 tokens for the benchmark
+// workloads: the small 64-sequence batch and the 256 x 512..4096 batch run best
+// unsplit, the 4 x 32k..128k and 128 x 1k..8k batches near 2048 tokens).
 int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, int request) {
   if (request < 0) return 0;
   const int max_tokens = maxNB * kBlock;
@@ -168,23 +173,33 @@ int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, i
   } else {
     const int G = Hq / Hkv;
     const int64_t units = static_cast<int64_t>(S) * Hkv * ((G + 7) / 8);
-    const int64_t resident = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D);
-    if (units >= 2 * resident) return 0;
-    const int64_t parts = (4 * resident + units - 1) / units;
-    int64_t pages = (maxNB + parts - 1) / parts;
-    pages = std::max<int64_t>(pages, 16);
+    const int64_t slots = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D);
+    const int64_t work = units * std::max(1, maxNB / 2);  // pages, assuming half-full tables
+    const int64_t pages = std::max<int64_t>(work / (4 * slots), 64);
+    if (2 * pages >= maxNB) return 0;
     P = static_cast<int>(pages * kBlock);
   }
   if (P >= max_tokens) return 0;
   return P;
 }
 
-size_t workspace_bytes_for(int S, int Hq, int D, int maxNB, int P) {
-  if (P <= 0) return 0;
+// Split-KV workspace: [arrival counters, one int per (sequence, kv head, head group)]
+// [partition (m, l): float2 per (sequence, head, partition)] [partition acc: D floats each],
+// each region starting on a 256-byte boundary.
+struct WsLayout {
+  size_t ml_off, acc_off, total;
+};
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+WsLayout workspace_layout(int S, int Hq, int Hkv, int D, int maxNB, int P) {
+  WsLayout L{0, 0, 0};
+  if (P <= 0) return L;
   const int64_t parts = (static_cast<int64_t>(maxNB) * kBlock + P - 1) / P;
   const int64_t rows = static_cast<int64_t>(S) * Hq * parts;
-  const size_t ml = (static_cast<size_t>(rows) * sizeof(float2) + 255) & ~static_cast<size_t>(255);
-  return ml + static_cast<size_t>(rows) * D * sizeof(float);
+  const int64_t units = static_cast<int64_t>(S) * Hkv * ((Hq / Hkv + 7) / 8);
+  L.ml_off = round256(static_cast<size_t>(units) * sizeof(int));
+  L.acc_off = L.ml_off + round256(static_cast<size_t>(rows) * sizeof(float2));
+  L.total = L.acc_off + static_cast<size_t>(rows) * D * sizeof(float);
+  return L;
 }
 
 // ------------------------------------------------------ internal workspace
@@ -329,12 +344,14 @@ PA_API int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int hea
   return PA_OK;
 }
 
-PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_size, int max_blocks_per_seq,
-                                       int partition_size) {
-  if (num_seqs < 0 || num_heads < 0 || head_size < 0 || max_blocks_per_seq < 0) return 0;
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                       int max_blocks_per_seq, int partition_size) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size < 0 ||
+      max_blocks_per_seq < 0)
+    return 0;
   const int P = partition_size > 0 ? (partition_size + kBlock - 1) / kBlock * kBlock : 0;
   if (P >= max_blocks_per_seq * kBlock) return 0;
-  return workspace_bytes_for(num_seqs, num_heads, head_size, max_blocks_per_seq, P);
+  return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, P).total;
 }
 
 namespace {
@@ -407,28 +424,28 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
 
   if (max_parts > 1) {
-    const size_t need = workspace_bytes_for(S, Hq, D, maxNB, P);
+    const WsLayout lay = workspace_layout(S, Hq, Hkv, D, maxNB, P);
     if (internal_ws) {
       int dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
       std::lock_guard<std::mutex> g(g_ws_mu);
       DevWorkspace &w = g_ws[dev];
-      if (w.bytes < need) {
+      if (w.bytes < lay.total) {
         if (w.ptr) cudaFreeAsync(w.ptr, st);
         w.ptr = nullptr;
         w.bytes = 0;
-        if (cudaMallocAsync(&w.ptr, need, st) != cudaSuccess) return PA_ERR_CUDA;
-        w.bytes = need;
+        if (cudaMallocAsync(&w.ptr, lay.total, st) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaMemsetAsync(w.ptr, 0, lay.total, st) != cudaSuccess) return PA_ERR_CUDA;
+        w.bytes = lay.total;
       }
       workspace = w.ptr;
       workspace_bytes = w.bytes;
     }
-    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PA_ERR_ALIGNMENT;
-    const int64_t rows = static_cast<int64_t>(S) * Hq * max_parts;
-    const size_t ml = (static_cast<size_t>(rows) * sizeof(float2) + 255) & ~static_cast<size_t>(255);
-    p.part_ml = static_cast<float2 *>(workspace);
-    p.part_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + ml);
+    p.counters = static_cast<int *>(workspace);
+    p.part_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + lay.ml_off);
+    p.part_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + lay.acc_off);
   }
 
   cudaError_t e;
@@ -450,13 +467,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
     if (kind == KIND_BF16 || kind == KIND_F16) e = launch_decode_mma_16(p, kind, tmK, tmV, st);
     else e = launch_decode_mma_fp8(p, kind, tmK, tmV, st);
   }
-  if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (max_parts > 1) {
-    ProfScope ps(PA_KERNEL_REDUCE, st);
-    e = launch_reduce(p, q->dtype, st);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
-  }
-  return PA_OK;
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -497,7 +508,7 @@ PA_API int pa_profile_enable(int on) {
 }
 
 PA_API int pa_profile_read(int kind, double *total_ms, long long *launches) {
-  if (kind < 0 || kind > 2) return PA_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 1) return PA_ERR_INVALID_ARG;
   Profiler &P = prof();
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
   {

@@ -40,12 +40,18 @@
 //
 // After the last page, each warp writes its (m, l, acc) to its own shared-memory
 // region; the CTA merges the W warp states with max/LSE rescaling and writes
-// either the normalised output (unsplit) or the partition's state to the
-// workspace for the split-KV reduce.
+// either the normalised output (a sequence with a single partition) or the
+// partition's state to the workspace, where the unit's last CTA merges all
+// partitions (pa_merge.cuh).
+//
+// The kernel is launched as a programmatic dependent of the previous grid on the
+// stream: it waits for that grid before its first global read, so its launch
+// overlaps the previous kernel's tail.
 #pragma once
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_merge.cuh"
 
 namespace pa {
 
@@ -87,7 +93,15 @@ __global__ void __launch_bounds__(W * 32)
   const bool split = p.max_parts > 1;
   using OutT = typename std::conditional<C::QBF16, __nv_bfloat16, __half>::type;
 
+  grid_dependency_wait();
+  const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
   const int len = __ldg(p.seq_lens + s);
+  int pid_reg = 0;  // lane i: physical block of my page (32 * chunk + i); chunk 0 read
+                    // speculatively (bounded by the table width) alongside seq_len
+  {
+    const int pg = part * p.pages_per_part + warp + lane * W;
+    if (pg < p.max_blocks) pid_reg = __ldg(bt + pg);
+  }
   if (len < 0 || len > p.max_blocks * kBlock) {
     if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
     return;
@@ -118,12 +132,10 @@ __global__ void __launch_bounds__(W * 32)
   __syncwarp();
 
   const uint64_t pol = policy_evict_first();
-  const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
   bool bad = false;
-  int pid_reg = 0;  // lane i: physical block of my page (32 * chunk + i)
 
   auto issue = [&](int kk) {  // whole warp; kk increases by one per call
-    if ((kk & 31) == 0) {
+    if ((kk & 31) == 0 && kk > 0) {
       const int k2 = kk + lane;
       pid_reg = (k2 < nmine) ? __ldg(bt + pb + warp + k2 * W) : 0;
     }
@@ -413,36 +425,42 @@ __global__ void __launch_bounds__(W * 32)
     }
   }
   const bool any_bad = __syncthreads_or(bad);
-  if (any_bad) return;
 
   const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.f;
-  for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
-    const int hh = i / D, d = i - hh * D;
-    float M = -INFINITY;
+  const int nparts = split ? (npages + p.pages_per_part - 1) / p.pages_per_part : 1;
+  const bool direct = nparts == 1;  // this CTA holds the whole sequence: write the output
+  if (!any_bad) {
+    for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
+      const int hh = i / D, d = i - hh * D;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
-      M = fmaxf(M, ml[2 * hh]);
-    }
-    float num = 0.f, den = 0.f;
+      for (int w = 0; w < W; ++w) {
+        const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
+        M = fmaxf(M, ml[2 * hh]);
+      }
+      float num = 0.f, den = 0.f;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
-      const float mw = ml[2 * hh];
-      const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-      den += sc * ml[2 * hh + 1];
-      num += sc * ml[16 + hh * D + d];
-    }
-    const int h = h0 + hh;
-    if (!split) {
-      OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h) * p.out_hs + d;
-      *o = OutT(den > 0.f ? num / den * vs : 0.f);
-    } else {
-      const int64_t row = (static_cast<int64_t>(s) * p.Hq + h) * p.max_parts + part;
-      p.part_acc[row * D + d] = num;
-      if (d == 0) p.part_ml[row] = make_float2(M, den);
+      for (int w = 0; w < W; ++w) {
+        const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
+        const float mw = ml[2 * hh];
+        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        den += sc * ml[2 * hh + 1];
+        num += sc * ml[16 + hh * D + d];
+      }
+      const int h = h0 + hh;
+      if (direct) {
+        OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h) * p.out_hs + d;
+        *o = OutT(den > 0.f ? num / den * vs : 0.f);
+      } else {
+        const int64_t row = (static_cast<int64_t>(s) * p.Hq + h) * p.max_parts + part;
+        p.part_acc[row * D + d] = num;
+        if (d == 0) p.part_ml[row] = make_float2(M, den);
+      }
     }
   }
+  // a CTA with an error still counts itself, so the unit's counter returns to zero
+  if (!direct) merge_if_last<OutT, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, vs,
+                                      C::THREADS);
 }
 
 }  // namespace pa

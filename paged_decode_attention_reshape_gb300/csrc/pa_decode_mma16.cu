@@ -14,8 +14,8 @@ cudaError_t go(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   const dim3 grid(p.max_parts, p.Hkv * p.HG, p.S);
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(p, tmK, tmV);
-  return cudaGetLastError();
+  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, p, tmK, tmV);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int KIND>

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -46,6 +48,7 @@ struct DecodeParams {
   const float *k_scale, *v_scale;      // nullable (1.0)
   int pages_per_part;                  // partition length in pages
   int max_parts;                       // partitions of the longest sequence (1 = unsplit)
+  int *counters;                       // [S, Hkv, HG] arrival counters of split units (zero between calls)
   float2 *part_ml;                     // [S, Hq, max_parts] (m in log2 units, l)
   float *part_acc;                     // [S, Hq, max_parts, D]
   int *err;                            // nullable
@@ -79,6 +82,21 @@ cudaError_t launch_decode_mma_16(const DecodeParams &p, int kind, const CUtensor
 cudaError_t launch_decode_mma_fp8(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                   cudaStream_t st);  // KIND_FP8_*
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st);
-cudaError_t launch_reduce(const DecodeParams &p, int out_dtype, cudaStream_t st);
+
+// Launch `kern` as a programmatic dependent of the previous work on `st`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 }  // namespace pa

@@ -71,6 +71,9 @@ __device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, float s) {
 
 template <int DT, bool FP8>
 __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
+  // the decode that usually follows waits for this grid's completion before its first
+  // read (griddepcontrol.wait), so it may be scheduled now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int IB = In<DT>::bytes;
   constexpr int EPP = 16 / IB;            // elements per 16-byte pack
   constexpr int CB = FP8 ? 1 : IB;        // cache element bytes

@@ -119,7 +119,7 @@ def to_gpu(c: Case, device="cuda") -> OnGpu:
     g.k_scale = torch.tensor([c.k_scale], dtype=torch.float32, device=device)
     g.v_scale = torch.tensor([c.v_scale], dtype=torch.float32, device=device)
     g.err = torch.zeros(1, dtype=torch.int32, device=device)
-    g.ws = torch.empty(64 << 20, dtype=torch.uint8, device=device)
+    g.ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)   # zero before first use
     return g
 
 

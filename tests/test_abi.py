@@ -138,9 +138,11 @@ def test_partition_plan_rules(L):
     assert pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, -1) == (0, 1)
     assert pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, 500) == (512, 256)
     assert pa.pa_decode_plan(4, 32, 8, 128, 8, pa.PA_BF16, 152, 512) == (0, 1)
-    # heuristic: a few long sequences are split, never below 256 tokens per partition
+    # heuristic: a few long sequences are split, never below 1024 tokens per partition
     P, n = pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, 0)
-    assert P >= 256 and P % 16 == 0 and n == -(-8192 * 16 // P) and n > 1
+    assert P >= 1024 and P % 16 == 0 and n == -(-8192 * 16 // P) and n > 1
+    # heuristic: short tables (partition >= half the width) are not split
+    assert pa.pa_decode_plan(64, 32, 8, 64, 128, pa.PA_BF16, 152, 0) == (0, 1)
     # heuristic: many (sequence, kv head) units fill the GPU without splitting
     assert pa.pa_decode_plan(4096, 32, 8, 128, 256, pa.PA_BF16, 152, 0) == (0, 1)
     # invalid arguments
@@ -149,13 +151,19 @@ def test_partition_plan_rules(L):
 
 
 def test_workspace_size(L):
-    S, Hq, D, MB = 4, 32, 128, 8192
-    assert pa.pa_decode_workspace_size(S, Hq, D, MB, 0) == 0
-    assert pa.pa_decode_workspace_size(S, Hq, D, MB, -1) == 0
+    S, Hq, Hkv, D, MB = 4, 32, 8, 128, 8192
+    assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, MB, 0) == 0
+    assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, MB, -1) == 0
+    assert pa.pa_decode_workspace_size(S, 30, Hkv, D, MB, 512) == 0           # Hq % Hkv != 0
     parts = -(-MB * 16 // 512)
     rows = S * Hq * parts
-    ml = (rows * 8 + 255) // 256 * 256
-    assert pa.pa_decode_workspace_size(S, Hq, D, MB, 512) == ml + rows * D * 4
+    r256 = lambda x: (x + 255) // 256 * 256
+    counters = r256(S * Hkv * 1 * 4)                                           # one per (seq, kv head, 8-head group)
+    assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, MB, 512) == counters + r256(rows * 8) + rows * D * 4
+    # 16 query heads per KV head -> two head groups per KV head
+    counters2 = r256(S * 2 * 2 * 4)
+    rows2 = S * 32 * parts
+    assert pa.pa_decode_workspace_size(S, 32, 2, D, MB, 512) == counters2 + r256(rows2 * 8) + rows2 * D * 4
 
 
 def test_check_device_error_rejects_null(L):
