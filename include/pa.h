@@ -182,6 +182,38 @@ int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, c
                  size_t workspace_bytes, int *device_error, pa_stream_t stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode_ex for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for callers that have no
+ * allocator where they run decode (a plugin that an inference runtime hands only
+ * its input and output buffers) or must not allocate there (a serving loop that
+ * has given all free device memory to its KV-cache pool, where an allocation can
+ * fail and cudaMalloc/cudaFree can synchronise the device).  It takes the same
+ * inputs and outputs as pa_decode_ex minus the workspace: the split-KV scratch is
+ * a fixed buffer of PA_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library, which
+ * every GPU that loads the library keeps until the process exits.  The call makes
+ * no cudaMalloc, cudaFree or other allocating call.
+ *
+ *   - A call whose plan needs more split-KV scratch than PA_NOALLOC_SCRATCH_BYTES
+ *     (pa_decode_workspace_size for the partition size it would use) returns
+ *     PA_ERR_WORKSPACE and launches nothing; use a larger partition_size, -1
+ *     (never split, needs no scratch) or pa_decode_ex.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress with that device current) and keeps it; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the one buffer, which keeps whatever the last
+ *     call left there.  Each call first clears, on its stream, the part that must
+ *     start at zero.  Calls that can overlap on the GPU (different streams without
+ *     ordering between them) race on the buffer and give wrong results.
+ * Returns the pa_decode_ex status codes.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int pa_decode_noalloc(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                      const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                      const float *k_scale, const float *v_scale, int partition_size, int *device_error,
+                      pa_stream_t stream);
+
+/*
  * pa_decode_plan -- host-only: the partition size pa_decode_ex would use.
  *   kv_dtype_code   pa_dtype of the cache; sm_count <= 0 queries the current device.
  *   partition_size  in: as for pa_decode_ex.  *partition_out: tokens per partition

@@ -29,8 +29,10 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED_DTYPE", 
           -4: "PA_ERR_WORKSPACE", -5: "PA_ERR_CUDA", -6: "PA_ERR_DEVICE_BOUNDS", -7: "PA_ERR_UNSUPPORTED_SHAPE",
           -8: "PA_ERR_DEVICE_TIMEOUT"}
 
-EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_ex", "pa_decode_plan", "pa_decode_workspace_size",
-           "pa_check_device_error", "pa_status_string", "pa_profile_enable", "pa_profile_read")
+EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_plan",
+           "pa_decode_workspace_size", "pa_check_device_error", "pa_status_string", "pa_profile_enable",
+           "pa_profile_read")
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _DT = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16, torch.uint8: PA_FP8_E4M3,
        torch.int32: PA_I32, torch.int64: PA_I64}
@@ -74,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.pa_decode.argtypes = [T, T, T, T, T, T, f32, i32, P]
             L.pa_decode_ex.restype = i32
             L.pa_decode_ex.argtypes = [T, T, T, T, T, T, f32, i32, P, P, i32, P, ctypes.c_size_t, P, P]
+            L.pa_decode_noalloc.restype = i32
+            L.pa_decode_noalloc.argtypes = [T, T, T, T, T, T, f32, i32, P, P, i32, P, P]
             L.pa_decode_plan.restype = i32
             L.pa_decode_plan.argtypes = [i32] * 8 + [ctypes.POINTER(i32), ctypes.POINTER(i32)]
             L.pa_decode_workspace_size.restype = ctypes.c_size_t
@@ -156,6 +160,18 @@ def pa_decode_ex(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, 
                             _ptr(v_scale), int(partition_size), _ptr(workspace), ws_bytes, _ptr(device_error),
                             _stream(stream))
     _check(rc, "pa_decode_ex")
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, num_kv_heads: int,
+                      k_scale=None, v_scale=None, partition_size: int = 0, device_error=None, stream=None) -> None:
+    """pa_decode_ex without a workspace argument: for callers that cannot allocate device memory
+    where they run decode.  Split-KV scratch comes from a fixed 32 MiB buffer inside the library,
+    shared by all calls on a device (calls that overlap on the GPU race on it); a problem needing
+    more than that raises PAError(PA_ERR_WORKSPACE)."""
+    args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(block_table), desc(seq_lens))
+    rc = lib().pa_decode_noalloc(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), _ptr(k_scale),
+                                 _ptr(v_scale), int(partition_size), _ptr(device_error), _stream(stream))
+    _check(rc, "pa_decode_noalloc")
 
 
 def pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kv_dtype_code,
