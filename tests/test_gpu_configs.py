@@ -1,0 +1,170 @@
+"""The five workloads at full size, staged exactly as bench.py stages them
+(NaN-poisoned pool, history written through the library, then one measured
+step: cache write + decode with the default partition plan), against the oracle.
+
+c1 and c2 are compared in full; c3-c5 on sampled (sequence, query head) outputs
+that the oracle computes one by one from the regenerated logical K/V; c4 also
+for each partition size of its sweep, and split against unsplit everywhere.
+Cache writes are compared bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from gpu_cases import assert_close
+from workloads import configs, data
+
+import paged_decode_attention_reshape_gb300 as pa
+
+pytestmark = pytest.mark.gpu
+B = 16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_decode_attention_reshape_gb300 import _build
+    _build.build()
+    pa.lib()
+    torch.cuda.set_device(0)
+
+
+def _bits16(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_heads(w, s, heads):
+    """fp64 oracle outputs [len(heads), D] of sequence s for the given query heads."""
+    kvh = sorted({h // w.G for h in heads})
+    K, V = data.logical_kv(w, s, kv_heads=kvh)
+    if w.kv_dtype == "e4m3":
+        L = K.shape[0]
+        ck = np.zeros((L, len(kvh), w.D), dtype=np.uint8)
+        cv = np.zeros((L, len(kvh), w.D), dtype=np.uint8)
+        oracle.write_flat(_bits16(K), "bf16", np.arange(L), ck, "e4m3", w.k_scale)
+        oracle.write_flat(_bits16(V), "bf16", np.arange(L), cv, "e4m3", w.v_scale)
+        Kv = oracle.cache_values(ck, "e4m3", w.k_scale)
+        Vv = oracle.cache_values(cv, "e4m3", w.v_scale)
+    else:
+        Kv, Vv = K.double().numpy(), V.double().numpy()
+    q = data.q(w, "cpu")[s].double().numpy()
+    out = []
+    for h in heads:
+        j = kvh.index(h // w.G)
+        out.append(oracle.dense_decode(q[h][None], Kv[:, j:j + 1], Vv[:, j:j + 1], w.scale)[0])
+    return np.stack(out)
+
+
+def step(st, P=0):
+    Pp, _, ws = bench.workspace_for(st, P)
+    bench.run_write(st)
+    bench.run_decode(st, P, ws)
+    torch.cuda.synchronize()
+    rc, bits = pa.pa_check_device_error(st.err)
+    assert rc == 0, (rc, bits)
+    return st.out.double().cpu().numpy()
+
+
+def check_step_write(st, rows=None):
+    """Cache rows at the step's slots (bit for bit) against the oracle's flat write of the step rows."""
+    w = st.w
+    valid = np.nonzero(w.step_slot >= 0)[0]
+    if rows is not None:
+        valid = valid[rows]
+    slots = torch.as_tensor(w.step_slot[valid])
+    blk, off = slots // B, slots % B
+    for cache, src, scale in ((st.k_cache, st.k_step, w.k_scale), (st.v_cache, st.v_step, w.v_scale)):
+        got = cache[blk.cuda(), :, off.cuda(), :].cpu()             # [n, Hkv, D]
+        rows_in = src[torch.as_tensor(valid).cuda()].cpu()
+        n = len(valid)
+        if w.cache_dtype == "e4m3":
+            ref = np.zeros((n, w.Hkv, w.D), dtype=np.uint8)
+            oracle.write_flat(_bits16(rows_in), "bf16", np.arange(n), ref, "e4m3", scale)
+            assert np.array_equal(got.numpy(), ref)
+        elif w.cache_dtype == "bf16":
+            ref = np.zeros((n, w.Hkv, w.D), dtype=np.uint16)
+            oracle.write_flat(_bits16(rows_in), "bf16", np.arange(n), ref, "bf16")
+            assert np.array_equal(_bits16(got), ref)
+        else:
+            ref = np.zeros((n, w.Hkv, w.D), dtype=np.float32)
+            oracle.write_flat(rows_in.numpy(), "f32", np.arange(n), ref, "f32")
+            assert np.array_equal(got.numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_c1_full():
+    w = configs.get("c1")
+    st = bench.stage(w)
+    for P in (0, -1, 16, 32):
+        got = step(st, P)
+        check_step_write(st)
+        for s in range(w.S):
+            assert_close(got[s], oracle_heads(w, s, range(w.Hq)), "c1 seq %d P=%d" % (s, P))
+    # the padding row (slot -1, NaN data) wrote nothing: the pool holds no NaN where a
+    # sequence lives, and the rest of the pool is still the NaN poison
+    kc = st.k_cache.cpu()
+    used = {int(b) for s in range(w.S) for b in w.block_table[s][:w.n_blocks_of(s)]}
+    for b in range(w.num_blocks):
+        if b in used:
+            continue
+        assert torch.isnan(kc[b]).all()
+
+
+def test_c2_full():
+    w = configs.get("c2")
+    st = bench.stage(w)
+    got = step(st, 0)
+    check_step_write(st)
+    for s in range(w.S):
+        assert_close(got[s], oracle_heads(w, s, range(w.Hq)), "c2 seq %d" % s)
+
+
+def test_c3_sampled():
+    w = configs.get("c3")
+    st = bench.stage(w)
+    got = step(st, 0)
+    check_step_write(st)
+    rng = np.random.default_rng(33)
+    for s in rng.choice(w.S, size=6, replace=False):
+        heads = sorted(rng.choice(w.Hq, size=4, replace=False).tolist())
+        assert_close(got[s][heads], oracle_heads(w, int(s), heads), "c3 seq %d" % s)
+
+
+def test_c4_sampled_over_partition_sizes():
+    w = configs.get("c4")
+    st = bench.stage(w)
+    outs = {P: step(st, P) for P in (0, 128, 256, 512, 1024, -1)}
+    rng = np.random.default_rng(44)
+    for s in range(w.S):
+        g = int(rng.integers(w.Hkv))
+        heads = [g * w.G, g * w.G + 1 + int(rng.integers(w.G - 1))]   # the outlier head of group g, and another
+        ref = oracle_heads(w, s, heads)
+        for P, got in outs.items():
+            assert_close(got[s][heads], ref, "c4 seq %d P=%d" % (s, P))
+    for P, got in outs.items():
+        assert_close(got, outs[-1], "c4 split %d vs unsplit" % P)
+
+
+def test_c5_fp8_write_and_sampled_decode():
+    w = configs.get("c5")
+    st = bench.stage(w)
+    got = step(st, 0)
+    rng = np.random.default_rng(55)
+    nvalid = int((w.step_slot >= 0).sum())
+    check_step_write(st, rows=np.sort(rng.choice(nvalid, size=512, replace=False)))
+    # padding rows (slot -1) wrote nothing: their positions still hold the history values
+    pad = np.nonzero(w.step_slot < 0)[0]
+    assert len(pad) == w.notes["padding_rows"] > 0
+    for s in np.unique(w.step_seq[pad]):
+        pos = w.step_pos[pad][w.step_seq[pad] == s]
+        K, V = data.history_rows(w, int(s), "cpu", positions=torch.as_tensor(pos))
+        slots = torch.as_tensor(w.slot_of(int(s), pos))
+        for cache, rows_in, scale in ((st.k_cache, K, w.k_scale), (st.v_cache, V, w.v_scale)):
+            ref = np.zeros((len(pos), w.Hkv, w.D), dtype=np.uint8)
+            oracle.write_flat(_bits16(rows_in), "bf16", np.arange(len(pos)), ref, "e4m3", scale)
+            gotc = cache[(slots // B).cuda(), :, (slots % B).cuda(), :].cpu().numpy()
+            assert np.array_equal(gotc, ref)
+    for s in rng.choice(w.S, size=6, replace=False):
+        heads = sorted(rng.choice(w.Hq, size=3, replace=False).tolist())
+        assert_close(got[s][heads], oracle_heads(w, int(s), heads), "c5 seq %d" % s)
+    # split (the plan) against unsplit on every output
+    assert_close(got, step(st, -1), "c5 split vs unsplit")
