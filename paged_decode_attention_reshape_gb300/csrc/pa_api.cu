@@ -147,6 +147,9 @@ int kind_of(int q_dtype, int cache_dtype) {
   return -1;
 }
 
+// Batches the tensor-core kernel runs longest-first (see lpt_sequence).
+bool longest_first(int kind, int S) { return kind != KIND_F32 && S <= 128; }
+
 int ctas_per_sm(int kind, int D) {
   if (kind == KIND_F32) return 4;
   const size_t smem = mma_smem(kind, D);
@@ -156,14 +159,19 @@ int ctas_per_sm(int kind, int D) {
 
 // Partition size in tokens (0 = unsplit).  The plan cannot read seq_lens (no
 // host sync), so it assumes lengths spread up to the block-table width (average
-// about half of it) and cuts that work into partitions of equal length so that
-// the GPU's resident CTA slots see about four waves.  A partition is never
-// shorter than 64 pages (1024 tokens), and when the partition would be at least
-// half the table width the call does not split at all: below those points the
-// per-CTA prologue and the partition merge cost more than the balance gains
-// (measured on GB300 over partition sizes 256..4096 tokens for the benchmark
-// workloads: the small 64-sequence batch and the 256 x 512..4096 batch run best
-// unsplit, the 4 x 32k..128k and 128 x 1k..8k batches near 2048 tokens).
+// about half of it).
+//  - Batches of at most kLptMax sequences run longest-first (the kernel ranks the
+//    lengths itself); when their (sequence, kv head, head group) units fill the
+//    GPU's resident CTA slots at least once, that order balances the load and the
+//    call does not split.
+//  - Otherwise the assumed work is cut into partitions of equal length so that
+//    the resident slots see about four waves.  A partition is never shorter than
+//    64 pages (1024 tokens), and when it would be at least half the table width
+//    the call does not split: below those points the per-CTA prologue and the
+//    partition merge cost more than the balance gains.
+// Fitted on GB300 to sweeps of 256..4096-token partitions over the benchmark
+// workloads (64 x 1..2048 tokens and 128 x 1k..8k run best unsplit, 256 x
+// 512..4096 unsplit or split alike, 4 x 32k..128k near 2048 tokens).
 int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, int request) {
   if (request < 0) return 0;
   const int max_tokens = maxNB * kBlock;
@@ -174,6 +182,7 @@ int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, i
     const int G = Hq / Hkv;
     const int64_t units = static_cast<int64_t>(S) * Hkv * ((G + 7) / 8);
     const int64_t slots = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D);
+    if (longest_first(kind, S) && units >= slots) return 0;
     const int64_t work = units * std::max(1, maxNB / 2);  // pages, assuming half-full tables
     const int64_t pages = std::max<int64_t>(work / (4 * slots), 64);
     if (2 * pages >= maxNB) return 0;
@@ -420,6 +429,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   p.pages_per_part = P > 0 ? P / kBlock : std::max(maxNB, 1);
   p.max_parts = max_parts;
   p.err = device_error;
+  p.lpt = longest_first(kind, S) ? 1 : 0;
   if (kind != KIND_FP8_BF16Q && kind != KIND_FP8_F16Q) p.k_scale = p.v_scale = nullptr;
   if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
 

@@ -127,8 +127,10 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
       }
     }
   }
-  if (!direct) merge_if_last<float, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, 1.f,
-                                       W * 32);
+  static_assert(sizeof(sm) >= 8 * kMergeSmemParts * 4, "merge weights reuse sm");
+  if (!direct)
+    merge_if_last<float, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, 1.f, W * 32,
+                            &sm[0][0][0]);
 }
 
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st) {

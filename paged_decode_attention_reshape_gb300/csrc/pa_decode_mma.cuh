@@ -70,9 +70,12 @@ struct MmaCfg {
   static constexpr int STAGEB = 2 * PAGEB;     // K page + V page
   static constexpr int KT = D / 16;            // k-steps of Q.K^T = d-tiles of P.V
   static constexpr int THREADS = W * 32;
-  static constexpr size_t SMEM = 1024 + static_cast<size_t>(W) * STAGES * STAGEB + W * STAGES * 8;
+  static constexpr size_t SCRATCH_OFF = static_cast<size_t>(W) * STAGES * STAGEB + W * STAGES * 8;
+  static constexpr size_t SMEM = 1024 + SCRATCH_OFF + kMmaScratch;
   static_assert(ROWB % 128 == 0, "page rows must be whole 128-byte swizzle spans");
   static_assert(STAGES * STAGEB >= 64 + 8 * D * 4, "warp region must hold the merge state");
+  static_assert(static_cast<size_t>(W) * STAGES * STAGEB >= 8 * kMergeSmemParts * 4, "merge weights");
+  static_assert(kMmaScratch >= kLptScratchBytes, "ranking scratch");
 };
 
 template <int KIND, int D, int W, int STAGES>
@@ -86,7 +89,7 @@ __global__ void __launch_bounds__(W * 32)
   uint8_t *const sgen = smem_raw + (sbase - raw_u32);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int s = blockIdx.z, part = blockIdx.x;
+  const int part = blockIdx.x;
   const int g = blockIdx.y / p.HG, hg = blockIdx.y - g * p.HG;
   const int h0 = g * p.G + hg * 8;      // first query head of this CTA
   const int ng = min(8, p.G - hg * 8);  // query heads in the group
@@ -94,6 +97,9 @@ __global__ void __launch_bounds__(W * 32)
   using OutT = typename std::conditional<C::QBF16, __nv_bfloat16, __half>::type;
 
   grid_dependency_wait();
+  const int s = p.lpt ? lpt_sequence(p.seq_lens, p.S, blockIdx.z, C::THREADS,
+                                    reinterpret_cast<int *>(sgen + C::SCRATCH_OFF))
+                      : static_cast<int>(blockIdx.z);
   const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
   const int len = __ldg(p.seq_lens + s);
   int pid_reg = 0;  // lane i: physical block of my page (32 * chunk + i); chunk 0 read
@@ -276,10 +282,8 @@ __global__ void __launch_bounds__(W * 32)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint32_t a[4];
-          a[0] = e4m3x2_to_f16x2(wa[j]);        // row ra,   d 4j, 4j+1
-          a[1] = e4m3x2_to_f16x2(wb[j]);        // row ra+8
-          a[2] = e4m3x2_to_f16x2(wa[j] >> 16);  // row ra,   d 4j+2, 4j+3
-          a[3] = e4m3x2_to_f16x2(wb[j] >> 16);  // row ra+8
+          e4m3x4_to_f16x2x2(wa[j], a[0], a[2]);  // row ra:   d 4j, 4j+1 | 4j+2, 4j+3
+          e4m3x4_to_f16x2x2(wb[j], a[1], a[3]);  // row ra+8
           if (j & 1) mma_f16(c1, a, qf[b * 8 + j][0], qf[b * 8 + j][1]);
           else mma_f16(c0, a, qf[b * 8 + j][0], qf[b * 8 + j][1]);
         }
@@ -305,12 +309,14 @@ __global__ void __launch_bounds__(W * 32)
     l1 = l1 * al1 + (p1 + p3);
     m0 = mn0;
     m1 = mn1;
+    if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {  // some running max moved
 #pragma unroll
-    for (int t = 0; t < C::KT; ++t) {
-      acc[t][0] *= al0;
-      acc[t][1] *= al1;
-      acc[t][2] *= al0;
-      acc[t][3] *= al1;
+      for (int t = 0; t < C::KT; ++t) {
+        acc[t][0] *= al0;
+        acc[t][1] *= al1;
+        acc[t][2] *= al0;
+        acc[t][3] *= al1;
+      }
     }
 
     // ---- P^T operand: hi + lo 16-bit halves, transposed in registers
@@ -381,10 +387,8 @@ __global__ void __launch_bounds__(W * 32)
           const uint32_t p01 = __byte_perm(x0[t >> 1], x1[t >> 1], sel);
           const uint32_t p23 = __byte_perm(x2[t >> 1], x3[t >> 1], sel);
           uint32_t a[4];
-          a[0] = e4m3x2_to_f16x2(p01);        // d0, tokens t0 t1
-          a[1] = e4m3x2_to_f16x2(p01 >> 16);  // d1, tokens t0 t1
-          a[2] = e4m3x2_to_f16x2(p23);        // d0, tokens t2 t3
-          a[3] = e4m3x2_to_f16x2(p23 >> 16);  // d1, tokens t2 t3
+          e4m3x4_to_f16x2x2(p01, a[0], a[1]);  // d0 | d1, tokens t0 t1
+          e4m3x4_to_f16x2x2(p23, a[2], a[3]);  // d0 | d1, tokens t2 t3
           mma_f16(acc[b * 8 + t], a, bh0, bh1);
           mma_f16(acc[b * 8 + t], a, bl0, bl1);
         }
@@ -459,8 +463,9 @@ __global__ void __launch_bounds__(W * 32)
     }
   }
   // a CTA with an error still counts itself, so the unit's counter returns to zero
-  if (!direct) merge_if_last<OutT, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, vs,
-                                      C::THREADS);
+  if (!direct)
+    merge_if_last<OutT, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, vs, C::THREADS,
+                           reinterpret_cast<float *>(sgen));
 }
 
 }  // namespace pa

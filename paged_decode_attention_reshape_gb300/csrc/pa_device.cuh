@@ -154,10 +154,15 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t x) {
   return __half22float2(v);
 }
 
-// Two E4M3 codes (low byte first) -> f16x2 (exact: every E4M3 value is an f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four E4M3 codes (byte 0 first) -> two f16x2: lo = (byte0, byte1), hi = (byte2, byte3),
+// each pair with its first byte in the low half.  Exact: every E4M3 value is an f16.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t &lo, uint32_t &hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
 }
 
 }  // namespace pa

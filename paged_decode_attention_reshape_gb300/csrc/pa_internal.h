@@ -52,6 +52,7 @@ struct DecodeParams {
   float2 *part_ml;                     // [S, Hq, max_parts] (m in log2 units, l)
   float *part_acc;                     // [S, Hq, max_parts, D]
   int *err;                            // nullable
+  int lpt;                             // 1: CTA row z takes the z-th longest sequence (S <= kLptMax)
   // fp32 path only: direct cache pointers and strides (elements)
   const float *kc, *vc;
   int64_t kc_s0, kc_s1, kc_s2, vc_s0, vc_s1, vc_s2;
@@ -72,9 +73,11 @@ constexpr int mma_warps(int kind, int D) { return (void)kind, (void)D, 4; }
 constexpr int mma_stages(int kind, int D) {
   return (kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) ? (D <= 128 ? 4 : 3) : (D <= 64 ? 4 : D <= 128 ? 3 : 2);
 }
+constexpr size_t kMmaScratch = 2048;  // sequence-order ranking scratch (after the barriers)
 constexpr size_t mma_smem(int kind, int D) {
   return 1024 + static_cast<size_t>(mma_warps(kind, D)) * mma_stages(kind, D) *
-                    (2 * kBlock * D * ((kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) ? 1 : 2) + 8);
+                    (2 * kBlock * D * ((kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) ? 1 : 2) + 8) +
+         kMmaScratch;
 }
 
 cudaError_t launch_decode_mma_16(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,

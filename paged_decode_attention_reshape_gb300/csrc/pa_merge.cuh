@@ -14,28 +14,36 @@
 // again at the end of every launch (the workspace contract: zero before first use).
 #pragma once
 
+#include <climits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 
+// Up to this many partitions the merge keeps the per-partition weights in shared memory.
+constexpr int kMergeSmemParts = 256;
+
+// smem_w: shared memory for 8 * kMergeSmemParts floats, free for reuse by now.
 template <typename OutT, int D>
 __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int unit, int h0, int ng, int nparts,
-                                              float vs, int threads) {
+                                              float vs, int threads, float *smem_w) {
   __shared__ int s_last;
-  __shared__ float s_md[8][2];
-  __syncthreads();  // every partial store of this CTA has been issued
+  float(*s_w)[kMergeSmemParts] = reinterpret_cast<float(*)[kMergeSmemParts]>(smem_w);  // weight per head, part
+  __syncthreads();  // every partial store of this CTA precedes thread 0's release below
   if (threadIdx.x == 0) {
-    __threadfence();  // ... and is visible device-wide before the arrival is counted
-    const int old = atomicAdd(p.counters + unit, 1);
+    int old;
+    // release: this CTA's partial states become visible before the arrival counts;
+    // acquire: the last arriver then sees every other partition's state
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + unit) : "memory");
     const int last = old == nparts - 1;
     if (last) atomicExch(p.counters + unit, 0);
     s_last = last;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = threads >> 5;
+  const bool in_smem = nparts <= kMergeSmemParts;
   for (int hh = warp; hh < ng; hh += nw) {
     const int64_t row0 = (static_cast<int64_t>(s) * p.Hq + h0 + hh) * p.max_parts;
     float M = -INFINITY;
@@ -45,29 +53,83 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int 
     float den = 0.f;
     for (int i = lane; i < nparts; i += 32) {
       const float2 v = __ldcg(p.part_ml + row0 + i);
-      den += (v.x == -INFINITY ? 0.f : ex2(v.x - M)) * v.y;
+      const float w = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+      den += w * v.y;
+      if (in_smem) s_w[hh][i] = w;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (lane == 0) {
-      s_md[hh][0] = M;
-      s_md[hh][1] = den;
+    const float inv = den > 0.f ? vs / den : 0.f;
+    if (in_smem) {
+      __syncwarp();
+      for (int i = lane; i < nparts; i += 32) s_w[hh][i] *= inv;
+    } else if (lane == 0) {
+      s_w[hh][0] = M;
+      s_w[hh][1] = inv;
     }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < ng * D; i += threads) {
     const int hh = i / D, d = i - hh * D;
-    const float M = s_md[hh][0], den = s_md[hh][1];
     const int64_t row0 = (static_cast<int64_t>(s) * p.Hq + h0 + hh) * p.max_parts;
-    float num = 0.f;
-    for (int q = 0; q < nparts; ++q) {
-      const float m = __ldcg(p.part_ml + row0 + q).x;
-      const float w = m == -INFINITY ? 0.f : ex2(m - M);
-      num += w * __ldcg(p.part_acc + (row0 + q) * D + d);
+    const float *acc = p.part_acc + row0 * D + d;
+    float r = 0.f;
+    if (in_smem) {
+      for (int q = 0; q < nparts; ++q) r += s_w[hh][q] * __ldcg(acc + static_cast<int64_t>(q) * D);
+    } else {
+      const float M = s_w[hh][0];
+      for (int q = 0; q < nparts; ++q) {
+        const float m = __ldcg(p.part_ml + row0 + q).x;
+        r += (m == -INFINITY ? 0.f : ex2(m - M)) * __ldcg(acc + static_cast<int64_t>(q) * D);
+      }
+      r *= s_w[hh][1];
     }
     OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + hh) * p.out_hs + d;
-    *o = static_cast<OutT>(den > 0.f ? num / den * vs : 0.f);
+    *o = static_cast<OutT>(r);
   }
+}
+
+// Longest-first order of sequences (for batches of at most kLptMax sequences).
+// The block scheduler starts CTAs in increasing blockIdx order, so when CTA row z
+// works on the z-th longest sequence, the long sequences start first and the last
+// wave is made of short ones (longest-processing-time-first list scheduling).
+// Warp 0 ranks all lengths with shuffles (ties by index) and the CTA takes the
+// sequence of rank `rank`.
+constexpr int kLptMax = 128;
+constexpr int kLptScratchBytes = 4 * kLptMax * 4;
+
+// smem_rank: shared memory for 4 * kLptMax ints.
+__device__ __forceinline__ int lpt_sequence(const int32_t *seq_lens, int S, int rank, int threads, int *smem_rank) {
+  int(*s_rank)[kLptMax] = reinterpret_cast<int(*)[kLptMax]>(smem_rank);
+  __shared__ int s_pick;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = threads >> 5;
+  int L[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    L[k] = i < S ? __ldg(seq_lens + i) : INT_MIN;
+  }
+  // warp w counts, for every i, the j in its 32-block(s) that come before i in the order
+  for (int jb = warp; jb < 4; jb += nw) {
+    int rk[4] = {0, 0, 0, 0};
+    const int Lb = jb == 0 ? L[0] : jb == 1 ? L[1] : jb == 2 ? L[2] : L[3];
+    if (jb * 32 < S) {
+#pragma unroll 8
+      for (int jj = 0; jj < 32; ++jj) {
+        const int Lj = __shfl_sync(0xffffffffu, Lb, jj);
+        const int j = jb * 32 + jj;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) rk[k] += (Lj > L[k]) | ((Lj == L[k]) & (j < lane + 32 * k));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s_rank[jb][lane + 32 * k] = rk[k];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < S; i += threads)
+    if (s_rank[0][i] + s_rank[1][i] + s_rank[2][i] + s_rank[3][i] == rank) s_pick = i;
+  __syncthreads();
+  return s_pick;
 }
 
 // Programmatic dependent launch: wait for the grid this one depends on (no-op
