@@ -163,15 +163,14 @@ int ctas_per_sm(int kind, int D) {
 //  - Batches of at most kLptMax sequences run longest-first (the kernel ranks the
 //    lengths itself); when their (sequence, kv head, head group) units fill the
 //    GPU's resident CTA slots at least once, that order balances the load and the
-//    call does not split.
-//  - Otherwise the assumed work is cut into partitions of equal length so that
-//    the resident slots see about four waves.  A partition is never shorter than
-//    64 pages (1024 tokens), and when it would be at least half the table width
-//    the call does not split: below those points the per-CTA prologue and the
-//    partition merge cost more than the balance gains.
-// Fitted on GB300 to sweeps of 256..4096-token partitions over the benchmark
-// workloads (64 x 1..2048 tokens and 128 x 1k..8k run best unsplit, 256 x
-// 512..4096 unsplit or split alike, 4 x 32k..128k near 2048 tokens).
+//    call does not split.  Any batch whose units fill the slots twice does not
+//    split either.
+//  - Otherwise the assumed work is cut into partitions of equal length, about two
+//    resident waves' worth, never shorter than 64 pages (1024 tokens): below that
+//    the per-CTA prologue and the partition merge cost more than the balance gains.
+// Fitted on GB300 to sweeps over partition sizes for the benchmark workloads:
+// 128 x 1k..8k tokens and 256 x 512..4096 run best unsplit, 64 x 1..2048 with its
+// longest sequences cut in two (1024), 4 x 32k..128k near 2048 tokens.
 int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, int request) {
   if (request < 0) return 0;
   const int max_tokens = maxNB * kBlock;
@@ -182,10 +181,10 @@ int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, i
     const int G = Hq / Hkv;
     const int64_t units = static_cast<int64_t>(S) * Hkv * ((G + 7) / 8);
     const int64_t slots = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D);
-    if (longest_first(kind, S) && units >= slots) return 0;
+    if ((longest_first(kind, S) && units >= slots) || units >= 2 * slots) return 0;
     const int64_t work = units * std::max(1, maxNB / 2);  // pages, assuming half-full tables
-    const int64_t pages = std::max<int64_t>(work / (4 * slots), 64);
-    if (2 * pages >= maxNB) return 0;
+    const int64_t pages = std::max<int64_t>(work / (2 * slots), 64);
+    if (pages >= maxNB) return 0;
     P = static_cast<int>(pages * kBlock);
   }
   if (P >= max_tokens) return 0;

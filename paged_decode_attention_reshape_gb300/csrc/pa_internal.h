@@ -70,9 +70,11 @@ cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, in
 // Tensor-core kernel shape per (kind, head size): warps per CTA and pipeline
 // stages per warp.  Shared memory = W * STAGES * 2 pages (+ alignment, barriers).
 constexpr int mma_warps(int kind, int D) { return (void)kind, (void)D, 4; }
-constexpr int mma_stages(int kind, int D) {
-  return (kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) ? (D <= 128 ? 4 : 3) : (D <= 64 ? 4 : D <= 128 ? 3 : 2);
-}
+// Two stages per warp: pages of 2-8 KiB and 4 warps give 35-131 KiB per CTA, so 6
+// (2 KiB pages), 3 (4 KiB) or 1 (8 KiB) CTAs fit per SM and a batch's units are
+// resident in fewer waves.  Measured on GB300: 3-4 stages with fewer CTAs per SM
+// were 3-10 % slower on every benchmark workload.
+constexpr int mma_stages(int kind, int D) { return (void)kind, (void)D, 2; }
 constexpr size_t kMmaScratch = 2048;  // sequence-order ranking scratch (after the barriers)
 constexpr size_t mma_smem(int kind, int D) {
   return 1024 + static_cast<size_t>(mma_warps(kind, D)) * mma_stages(kind, D) *

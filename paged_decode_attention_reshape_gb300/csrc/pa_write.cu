@@ -6,11 +6,15 @@
 // conversion is a copy, or scale-and-convert for an FP8 cache.
 //
 // GB300 design: the work item is one 16-byte pack of one (token, kv head) row,
-// for K and V together.  Adjacent threads take adjacent packs of the source
-// (fully coalesced reads), and each destination (block, head, offset) row is a
-// contiguous run of D * elem bytes in the HND cache, so a warp's stores cover
-// whole 32-byte sectors.  Sources are read once with no L1 allocation.  The grid
-// is a multiple of the SM count, grid-striding over all packs.
+// for K and V together.  A 256-thread block covers whole tokens (adjacent threads
+// take adjacent packs of the source: fully coalesced reads), so each thread's
+// token and pack indices are fixed and the loop is a stride over tokens; each
+// destination (block, head, offset) row is a contiguous run of D * elem bytes in
+// the HND cache, so a warp's stores cover whole 32-byte sectors.  Sources are read
+// once with no L1 allocation.  The grid is at most 8 CTAs per SM, grid-striding
+// over tokens.  The E4M3 path divides by the per-tensor scale with a
+// reciprocal-based, correctly rounded quotient (Divisor below), the same value as
+// an IEEE division.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -47,25 +51,57 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&x)[16 / In<DT>::
   }
 }
 
-// E4M3 code pair of (a / s, b / s): IEEE division rounded to nearest, then
+// The correctly rounded quotient x / s for one divisor s shared by a whole tensor.
+// With y = RN(1/s): q0 = RN(x y) is within 1.5 ulp of x/s; one correction
+// q1 = RN(q0 + (x - q0 s) y) brings it within 1 ulp, and then (Markstein's theorem:
+// y within half an ulp of 1/s, q1 within one ulp of x/s, residual x - q1 s exact by
+// FMA) q2 = RN(q1 + (x - q1 s) y) is RN(x/s).  The theorem needs the operands and the
+// residuals away from underflow and overflow, so zero, tiny, huge, infinite or NaN x
+// (and divisors outside [2^-40, 2^40]) take the general IEEE division instead.
+struct Divisor {
+  float s, y;
+  bool fast;
+  __device__ __forceinline__ float div(float x) const {
+    const float ax = fabsf(x);
+    if (fast && ax >= 0x1p-80f && ax <= 0x1p80f) {  // false for NaN
+      float q = __fmul_rn(x, y);
+      float r = __fmaf_rn(-q, s, x);
+      q = __fmaf_rn(r, y, q);
+      r = __fmaf_rn(-q, s, x);
+      return __fmaf_rn(r, y, q);
+    }
+    return __fdiv_rn(x, s);
+  }
+};
+
+__device__ __forceinline__ Divisor make_divisor(float s) {
+  Divisor d;
+  d.s = s;
+  d.y = __frcp_rn(s);
+  const float as = fabsf(s);
+  d.fast = as >= 0x1p-40f && as <= 0x1p40f;
+  return d;
+}
+
+// E4M3 code pair of (a / s, b / s): correctly rounded fp32 quotient, then
 // round-to-nearest-even with saturation (cvt ... satfinite); low byte = a.
-__device__ __forceinline__ uint32_t quant2(float a, float b, float s) {
-  const float2 y = make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+__device__ __forceinline__ uint32_t quant2(float a, float b, const Divisor &dv) {
+  const float2 y = make_float2(dv.div(a), dv.div(b));
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3));
 }
 
 template <int DT>
-__device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, float s) {
+__device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, const Divisor &dv) {
   constexpr int E = 16 / In<DT>::bytes;
   float x[E];
   unpack8<DT>(v, x);
   if constexpr (E == 8) {
     uint2 o;
-    o.x = quant2(x[0], x[1], s) | (quant2(x[2], x[3], s) << 16);
-    o.y = quant2(x[4], x[5], s) | (quant2(x[6], x[7], s) << 16);
+    o.x = quant2(x[0], x[1], dv) | (quant2(x[2], x[3], dv) << 16);
+    o.y = quant2(x[4], x[5], dv) | (quant2(x[6], x[7], dv) << 16);
     *reinterpret_cast<uint2 *>(dst) = o;
   } else {
-    *reinterpret_cast<uint32_t *>(dst) = quant2(x[0], x[1], s) | (quant2(x[2], x[3], s) << 16);
+    *reinterpret_cast<uint32_t *>(dst) = quant2(x[0], x[1], dv) | (quant2(x[2], x[3], dv) << 16);
   }
 }
 
@@ -78,36 +114,42 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
   constexpr int EPP = 16 / IB;            // elements per 16-byte pack
   constexpr int CB = FP8 ? 1 : IB;        // cache element bytes
   const int ppr = p.D / EPP;              // packs per (token, head) row
-  const int64_t per_tok = static_cast<int64_t>(p.Hkv) * ppr;
-  const int64_t total = p.T * per_tok;
+  const int per_tok = p.Hkv * ppr;        // packs per token
+  // thread -> (token within the block's rows, pack within the token), fixed for the kernel;
+  // a token wider than the block is covered by an inner loop over packs
+  const int width = min(per_tok, 256);
+  const int rows = 256 / width;
+  const int tl = threadIdx.x / width;
+  const int j0 = threadIdx.x - tl * width;
   float ks = 1.f, vs = 1.f;
   if (FP8) {
     if (p.k_scale) ks = __ldg(p.k_scale);
     if (p.v_scale) vs = __ldg(p.v_scale);
   }
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = i / per_tok;
-    const int r = static_cast<int>(i - t * per_tok);
-    const int h = r / ppr;
-    const int64_t e = static_cast<int64_t>(r - h * ppr) * EPP;
+  const Divisor kdiv = make_divisor(ks), vdiv = make_divisor(vs);
+  if (tl >= rows) return;  // spare threads when 256 is not a multiple of per_tok
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * rows + tl; t < p.T; t += static_cast<int64_t>(gridDim.x) * rows) {
     const int64_t slot = __ldg(p.slot_mapping + t);
     if (slot < 0) continue;  // padding row: no destination
     if (slot >= p.num_slots) {
-      if (p.err) atomicOr(p.err, kErrSlot);
+      if (p.err && j0 == 0) atomicOr(p.err, kErrSlot);
       continue;
     }
     const int64_t blk = slot / kBlock, off = slot % kBlock;
-    const uint4 kv = ld_once(static_cast<const char *>(p.key) + (t * p.key_ts + h * p.key_hs + e) * IB);
-    const uint4 vv = ld_once(static_cast<const char *>(p.value) + (t * p.val_ts + h * p.val_hs + e) * IB);
-    char *kd = static_cast<char *>(p.k_cache) + (blk * p.kc_s0 + h * p.kc_s1 + off * p.kc_s2 + e) * CB;
-    char *vd = static_cast<char *>(p.v_cache) + (blk * p.vc_s0 + h * p.vc_s1 + off * p.vc_s2 + e) * CB;
-    if constexpr (!FP8) {
-      *reinterpret_cast<uint4 *>(kd) = kv;
-      *reinterpret_cast<uint4 *>(vd) = vv;
-    } else {
-      store_fp8<DT>(kd, kv, ks);
-      store_fp8<DT>(vd, vv, vs);
+    for (int j = j0; j < per_tok; j += 256) {
+      const int h = j / ppr;
+      const int64_t e = static_cast<int64_t>(j - h * ppr) * EPP;
+      const uint4 kv = ld_once(static_cast<const char *>(p.key) + (t * p.key_ts + h * p.key_hs + e) * IB);
+      const uint4 vv = ld_once(static_cast<const char *>(p.value) + (t * p.val_ts + h * p.val_hs + e) * IB);
+      char *kd = static_cast<char *>(p.k_cache) + (blk * p.kc_s0 + h * p.kc_s1 + off * p.kc_s2 + e) * CB;
+      char *vd = static_cast<char *>(p.v_cache) + (blk * p.vc_s0 + h * p.vc_s1 + off * p.vc_s2 + e) * CB;
+      if constexpr (!FP8) {
+        *reinterpret_cast<uint4 *>(kd) = kv;
+        *reinterpret_cast<uint4 *>(vd) = vv;
+      } else {
+        store_fp8<DT>(kd, kv, kdiv);
+        store_fp8<DT>(vd, vv, vdiv);
+      }
     }
   }
 }
@@ -115,13 +157,13 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
 template <int DT, bool FP8>
 cudaError_t launch_one(const WriteParams &p, int sm_count, cudaStream_t st) {
   constexpr int EPP = 16 / In<DT>::bytes;
-  const int64_t total = p.T * p.Hkv * (p.D / EPP);
-  const int threads = 256;
-  int64_t blocks = (total + threads - 1) / threads;
+  const int per_tok = p.Hkv * (p.D / EPP);
+  const int rows = 256 / (per_tok < 256 ? per_tok : 256);
+  int64_t blocks = (p.T + rows - 1) / rows;
   const int64_t cap = static_cast<int64_t>(sm_count) * 8;  // 8 x 256 threads per SM, grid-stride
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  write_kernel<DT, FP8><<<static_cast<unsigned>(blocks), threads, 0, st>>>(p);
+  write_kernel<DT, FP8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -141,8 +141,10 @@ def test_partition_plan_rules(L):
     # heuristic: a few long sequences are split, never below 1024 tokens per partition
     P, n = pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, 0)
     assert P >= 1024 and P % 16 == 0 and n == -(-8192 * 16 // P) and n > 1
-    # heuristic: short tables (partition >= half the width) are not split
-    assert pa.pa_decode_plan(64, 32, 8, 64, 128, pa.PA_BF16, 152, 0) == (0, 1)
+    # heuristic: a partition as long as the table is no split
+    assert pa.pa_decode_plan(64, 32, 8, 64, 64, pa.PA_BF16, 152, 0) == (0, 1)
+    # heuristic: a longest-first batch whose units fill the resident slots is not split
+    assert pa.pa_decode_plan(128, 64, 8, 128, 512, pa.PA_FP8_E4M3, 152, 0) == (0, 1)
     # heuristic: many (sequence, kv head) units fill the GPU without splitting
     assert pa.pa_decode_plan(4096, 32, 8, 128, 256, pa.PA_BF16, 152, 0) == (0, 1)
     # invalid arguments
