@@ -158,12 +158,17 @@ int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, cons
  *
  *   k_scale, v_scale  device fp32 per-tensor dequantisation scales for an FP8 cache
  *                     (K and V element values are code_value * scale); NULL = 1.0.
- *   partition_size    KV tokens per split-KV partition: 0 = chosen by the
- *                     library's measured heuristic (pa_decode_plan), -1 = never
- *                     split, > 0 = that many tokens (rounded up to a multiple of 16).
+ *   partition_size    how the KV range of a sequence is split: 0 = chosen by the
+ *                     library's measured heuristic (pa_decode_plan); -1 = never split;
+ *                     > 0 = partitions of that many tokens (rounded up to a multiple of
+ *                     16), merged through the workspace; -2, -4 or -8 = every sequence
+ *                     cut into 2, 4 or 8 equal parts processed by the CTAs of one
+ *                     thread-block cluster and merged through distributed shared
+ *                     memory (no workspace).
  *   workspace,        device memory for split-KV partition states; at least
  *   workspace_bytes   pa_decode_workspace_size(...) bytes for the partition size
- *                     the call ends up using (0 bytes when it does not split).
+ *                     the call ends up using (0 bytes when it does not split or
+ *                     uses the cluster split).
  *                     NULL with workspace_bytes == 0 is fine for the unsplit path.
  *                     Zero-fill it once before its first use: it holds per-unit
  *                     arrival counters that every call leaves at zero again.  The
@@ -214,11 +219,12 @@ int pa_decode_noalloc(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cac
                       pa_stream_t stream);
 
 /*
- * pa_decode_plan -- host-only: the partition size pa_decode_ex would use.
+ * pa_decode_plan -- host-only: the split pa_decode_ex would use.
  *   kv_dtype_code   pa_dtype of the cache; sm_count <= 0 queries the current device.
- *   partition_size  in: as for pa_decode_ex.  *partition_out: tokens per partition
- *                   (0 = unsplit); *num_partitions_out: partitions of the longest
- *                   possible sequence (max_blocks_per_seq * 16 tokens).
+ *   partition_size  in: as for pa_decode_ex.  *partition_out: tokens per fixed
+ *                   partition, 0 = unsplit, or -C for the cluster split into C parts;
+ *                   *num_partitions_out: partitions of the longest possible sequence
+ *                   (max_blocks_per_seq * 16 tokens), or C.
  * Returns PA_OK or PA_ERR_INVALID_ARG.  No device memory is touched.
  */
 int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_blocks_per_seq,

@@ -191,6 +191,31 @@ int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, i
   return P;
 }
 
+// The full plan: fixed-size partitions (P tokens, merged through the workspace by the
+// last-arriving CTA) or, on request only (request = -2, -4 or -8), a cluster split:
+// each unit cut into C equal parts whose CTAs form one thread-block cluster and merge
+// through distributed shared memory, with no workspace.  The heuristic does not pick
+// the cluster split: cutting every unit (short ones too) multiplies the CTAs beyond the
+// resident slots, and on GB300 that cost more than the shorter critical path saved
+// (64 x 1..2048 tokens: 33.2 us unsplit, 34.3 / 42.1 / 56.1 us for C = 2 / 4 / 8,
+// 32.9 us with 1024-token partitions).
+struct Plan {
+  int P;        // tokens per fixed partition (0 = none)
+  int cluster;  // parts per unit of the cluster split (0 = none)
+  int status;
+};
+Plan make_plan(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, int request) {
+  Plan pl{0, 0, PA_OK};
+  if (request <= -2) {
+    const int C = -request;
+    if (C != 2 && C != 4 && C != 8) pl.status = PA_ERR_INVALID_ARG;
+    else pl.cluster = C;
+    return pl;
+  }
+  pl.P = plan_partition(S, Hq, Hkv, D, maxNB, kind, sm, request);
+  return pl;
+}
+
 // Split-KV workspace: [arrival counters, one int per (sequence, kv head, head group)]
 // [partition (m, l): float2 per (sequence, head, partition)] [partition acc: D floats each],
 // each region starting on a 256-byte boundary.
@@ -344,11 +369,12 @@ PA_API int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int hea
   }
   if (sm_count <= 0) sm_count = device_sm_count();
   if (sm_count <= 0) return PA_ERR_CUDA;
-  const int P = plan_partition(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kind, sm_count,
-                               partition_size);
-  if (partition_out) *partition_out = P;
+  const Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kind, sm_count,
+                            partition_size);
+  if (pl.status != PA_OK) return pl.status;
+  if (partition_out) *partition_out = pl.cluster > 1 ? -pl.cluster : pl.P;
   if (num_partitions_out)
-    *num_partitions_out = P > 0 ? (max_blocks_per_seq * kBlock + P - 1) / P : 1;
+    *num_partitions_out = pl.cluster > 1 ? pl.cluster : pl.P > 0 ? (max_blocks_per_seq * kBlock + pl.P - 1) / pl.P : 1;
   return PA_OK;
 }
 
@@ -400,8 +426,10 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   const int maxNB = static_cast<int>(block_table->shape[1]);
   const int sm = device_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
-  const int P = plan_partition(S, Hq, Hkv, D, maxNB, kind, sm, partition_size);
-  const int max_parts = P > 0 ? (maxNB * kBlock + P - 1) / P : 1;
+  const Plan pl = make_plan(S, Hq, Hkv, D, maxNB, kind, sm, partition_size);
+  if (pl.status != PA_OK) return pl.status;
+  const int P = pl.P;
+  const int max_parts = pl.cluster > 1 ? pl.cluster : P > 0 ? (maxNB * kBlock + P - 1) / P : 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   DecodeParams p{};
@@ -427,12 +455,19 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   p.v_scale = v_scale;
   p.pages_per_part = P > 0 ? P / kBlock : std::max(maxNB, 1);
   p.max_parts = max_parts;
+  p.cluster = pl.cluster;
   p.err = device_error;
-  p.lpt = longest_first(kind, S) ? 1 : 0;
+  {
+    // Order the batch longest-first only when its CTAs cannot all be resident at once:
+    // with every CTA resident from the start the order buys nothing and the ranking
+    // (a read of every length plus two block barriers) sits on each CTA's critical path.
+    const int64_t ctas = static_cast<int64_t>(S) * Hkv * p.HG * max_parts;
+    p.lpt = (longest_first(kind, S) && ctas > static_cast<int64_t>(sm) * ctas_per_sm(kind, D)) ? 1 : 0;
+  }
   if (kind != KIND_FP8_BF16Q && kind != KIND_FP8_F16Q) p.k_scale = p.v_scale = nullptr;
   if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
 
-  if (max_parts > 1) {
+  if (max_parts > 1 && pl.cluster <= 1) {
     const WsLayout lay = workspace_layout(S, Hq, Hkv, D, maxNB, P);
     if (internal_ws) {
       int dev = 0;

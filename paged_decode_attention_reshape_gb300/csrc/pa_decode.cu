@@ -30,9 +30,11 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
     return;
   }
   const int npages = (len + kBlock - 1) / kBlock;
-  const int pb = part * p.pages_per_part;
-  const int pe = min(npages, pb + p.pages_per_part);
-  if (pb >= pe) {
+  const bool clustered = p.cluster > 1;  // rank `part` of a cluster splitting the unit equally
+  const int pb = clustered ? static_cast<int>(static_cast<int64_t>(part) * npages / p.cluster) : part * p.pages_per_part;
+  const int pe = clustered ? static_cast<int>(static_cast<int64_t>(part + 1) * npages / p.cluster)
+                           : min(npages, pb + p.pages_per_part);
+  if (pb >= pe && !clustered) {
     if (!split && part == 0)
       for (int i = threadIdx.x; i < ng * D; i += W * 32)
         static_cast<float *>(p.out)[s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D] = 0.f;
@@ -100,6 +102,31 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
     }
   }
   const bool any_bad = __syncthreads_or(bad);
+  if (clustered) {
+    // CTA state in place over warp 0's slots (each element is read and overwritten by one thread)
+    __shared__ float2 cmd[8];
+    __shared__ int cbad;
+    if (!any_bad) {
+      for (int i = threadIdx.x; i < ng * D; i += W * 32) {
+        const int hh = i / D, d = i - hh * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, sm[w][hh][D]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float mw = sm[w][hh][D];
+          const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          den += sc * sm[w][hh][D + 1];
+          num += sc * sm[w][hh][d];
+        }
+        sm[0][hh][d] = num;
+        if (d == 0) cmd[hh] = make_float2(M, den);
+      }
+    }
+    cluster_merge_write<float, D>(p, s, h0, ng, 1.f, any_bad, &sm[0][0][0], D + 2, cmd, &cbad, W * 32);
+    return;
+  }
   const int nparts = split ? (npages + p.pages_per_part - 1) / p.pages_per_part : 1;
   const bool direct = nparts == 1;
   if (!any_bad) {
@@ -137,9 +164,9 @@ cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st) {
   const dim3 grid(p.max_parts, p.Hkv * p.HG, p.S);
   cudaError_t e;
   switch (p.D) {
-    case 64: e = launch_pdl(decode_f32_kernel<64, 4>, grid, dim3(128), 0, st, p); break;
-    case 128: e = launch_pdl(decode_f32_kernel<128, 4>, grid, dim3(128), 0, st, p); break;
-    case 256: e = launch_pdl(decode_f32_kernel<256, 2>, grid, dim3(64), 0, st, p); break;
+    case 64: e = launch_pdl(decode_f32_kernel<64, 4>, grid, dim3(128), 0, st, p.cluster, p); break;
+    case 128: e = launch_pdl(decode_f32_kernel<128, 4>, grid, dim3(128), 0, st, p.cluster, p); break;
+    case 256: e = launch_pdl(decode_f32_kernel<256, 2>, grid, dim3(64), 0, st, p.cluster, p); break;
     default: return cudaErrorInvalidValue;
   }
   return e != cudaSuccess ? e : cudaGetLastError();

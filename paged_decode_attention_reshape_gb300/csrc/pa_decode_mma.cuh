@@ -96,26 +96,56 @@ __global__ void __launch_bounds__(W * 32)
   const bool split = p.max_parts > 1;
   using OutT = typename std::conditional<C::QBF16, __nv_bfloat16, __half>::type;
 
+  // Warm L2 with the metadata this launch reads on its critical path: CTA row z
+  // prefetches sequence z's slice of the block table (the first head group only) and
+  // its query heads (the first partition only); together the rows cover every
+  // sequence, whichever row ends up working on it.  A prefetch returns no data, so it
+  // may run before the wait on the previous grid.
+  if (warp == 0) {
+    const int z = blockIdx.z;
+    if (blockIdx.y == 0) {
+      const int pg0 = p.cluster > 1 ? part * p.max_blocks / p.cluster : part * p.pages_per_part;
+      const int pg1 = p.cluster > 1 ? (part + 1) * p.max_blocks / p.cluster : min(p.max_blocks, pg0 + p.pages_per_part);
+      const int32_t *row = p.block_table + static_cast<int64_t>(z) * p.bt_ss;
+      for (int pg = pg0 + lane * 32; pg < pg1; pg += 32 * 32) prefetch_l2(row + pg);
+    }
+    if (part == 0) {
+      const char *qr = static_cast<const char *>(p.q) +
+                       (static_cast<int64_t>(z) * p.q_ss + static_cast<int64_t>(h0) * p.q_hs) * 2;
+      const int bytes = ng * D * 2;
+      if (lane * 128 < bytes && p.q_hs == D) prefetch_l2(qr + lane * 128);
+    }
+  }
   grid_dependency_wait();
   const int s = p.lpt ? lpt_sequence(p.seq_lens, p.S, blockIdx.z, C::THREADS,
                                     reinterpret_cast<int *>(sgen + C::SCRATCH_OFF))
                       : static_cast<int>(blockIdx.z);
   const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
   const int len = __ldg(p.seq_lens + s);
-  int pid_reg = 0;  // lane i: physical block of my page (32 * chunk + i); chunk 0 read
-                    // speculatively (bounded by the table width) alongside seq_len
-  {
+  const bool clustered = p.cluster > 1;  // rank `part` of a cluster splitting the unit equally
+  int pid_reg = 0;  // lane i: physical block of my page (32 * chunk + i); with fixed-size
+                    // partitions chunk 0 is read speculatively (bounded by the table width)
+                    // alongside seq_len
+  if (!clustered) {
     const int pg = part * p.pages_per_part + warp + lane * W;
     if (pg < p.max_blocks) pid_reg = __ldg(bt + pg);
   }
-  if (len < 0 || len > p.max_blocks * kBlock) {
+  if (len < 0 || len > p.max_blocks * kBlock) {  // (all ranks of a cluster see the same length)
     if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
     return;
   }
   const int npages = (len + kBlock - 1) / kBlock;
-  const int pb = part * p.pages_per_part;
-  const int pe = min(npages, pb + p.pages_per_part);
-  if (pb >= pe) {
+  int pb, pe;
+  if (clustered) {
+    pb = static_cast<int>(static_cast<int64_t>(part) * npages / p.cluster);
+    pe = static_cast<int>(static_cast<int64_t>(part + 1) * npages / p.cluster);
+    const int pg = pb + warp + lane * W;
+    if (pg < pe) pid_reg = __ldg(bt + pg);
+  } else {
+    pb = part * p.pages_per_part;
+    pe = min(npages, pb + p.pages_per_part);
+  }
+  if (pb >= pe && !clustered) {  // (an empty cluster rank stays: it takes part in the merge)
     if (!split && part == 0) {  // empty sequence: zero output rows
       for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
         OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D;
@@ -431,6 +461,34 @@ __global__ void __launch_bounds__(W * 32)
   const bool any_bad = __syncthreads_or(bad);
 
   const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.f;
+  if (clustered) {
+    // CTA state in place: element (hh, d) of warp 0's accumulator region is read only by
+    // the thread that overwrites it; (max, exp-sum) per head go to the scratch area
+    float *cs = reinterpret_cast<float *>(sgen) + 16;
+    float2 *cmd = reinterpret_cast<float2 *>(sgen + C::SCRATCH_OFF);
+    if (!any_bad) {
+      for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
+        const int hh = i / D, d = i - hh * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB)[2 * hh]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
+          const float mw = ml[2 * hh];
+          const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          den += sc * ml[2 * hh + 1];
+          num += sc * ml[16 + hh * D + d];
+        }
+        cs[hh * D + d] = num;
+        if (d == 0) cmd[hh] = make_float2(M, den);
+      }
+    }
+    cluster_merge_write<OutT, D>(p, s, h0, ng, vs, any_bad, cs, D, cmd, reinterpret_cast<int *>(cmd + 8),
+                                 C::THREADS);
+    return;
+  }
   const int nparts = split ? (npages + p.pages_per_part - 1) / p.pages_per_part : 1;
   const bool direct = nparts == 1;  // this CTA holds the whole sequence: write the output
   if (!any_bad) {

@@ -13,8 +13,11 @@ cudaError_t go(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap 
   auto kern = decode_mma_kernel<KIND, D, W, ST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
+  // same shared/L1 split as the cache write that usually precedes it (no reconfiguration)
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   const dim3 grid(p.max_parts, p.Hkv * p.HG, p.S);
-  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, p, tmK, tmV);
+  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p, tmK, tmV);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

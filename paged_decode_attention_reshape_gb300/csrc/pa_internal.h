@@ -47,7 +47,8 @@ struct DecodeParams {
   float scale_log2;                    // softmax scale * log2(e)
   const float *k_scale, *v_scale;      // nullable (1.0)
   int pages_per_part;                  // partition length in pages
-  int max_parts;                       // partitions of the longest sequence (1 = unsplit)
+  int max_parts;                       // partitions of the longest sequence (1 = unsplit); = cluster if > 1
+  int cluster;                         // > 1: cluster split, each unit cut into `cluster` equal parts
   int *counters;                       // [S, Hkv, HG] arrival counters of split units (zero between calls)
   float2 *part_ml;                     // [S, Hq, max_parts] (m in log2 units, l)
   float *part_acc;                     // [S, Hq, max_parts, D]
@@ -88,19 +89,29 @@ cudaError_t launch_decode_mma_fp8(const DecodeParams &p, int kind, const CUtenso
                                   cudaStream_t st);  // KIND_FP8_*
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st);
 
-// Launch `kern` as a programmatic dependent of the previous work on `st`.
+// Launch `kern` as a programmatic dependent of the previous work on `st`, in
+// thread-block clusters of `cluster_x` CTAs along x when cluster_x > 1.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args) {
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_x,
+                       Args &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 

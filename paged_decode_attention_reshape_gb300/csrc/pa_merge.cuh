@@ -89,6 +89,44 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int 
   }
 }
 
+// The cluster split: the C CTAs of a thread-block cluster each take an equal share
+// of one (sequence, kv head, head group) unit's pages.  Each CTA has already stored
+// its state in its own shared memory -- the unnormalised output cs[hh * cs_stride + d]
+// and (max in log2 units, exp-sum) cmd[hh] -- and here, after a cluster barrier, CTA
+// rank r merges the d-slice [r D/C, (r+1) D/C) of every head, reading the C states
+// through distributed shared memory, and writes the output.  A second barrier keeps
+// each CTA's shared memory alive until the others have read it.  No global memory
+// and no workspace are involved.
+template <typename OutT, int D>
+__device__ __forceinline__ void cluster_merge_write(const DecodeParams &p, int s, int h0, int ng, float vs, bool bad,
+                                                    const float *cs, int cs_stride, const float2 *cmd, int *cbad,
+                                                    int threads) {
+  if (threadIdx.x == 0) *cbad = bad ? 1 : 0;
+  cluster_sync();
+  const int C = p.cluster;
+  const int r = static_cast<int>(cluster_rank());
+  int anybad = 0;
+  for (int j = 0; j < C; ++j) anybad |= ld_dsmem_s32(dsmem_addr(cbad, j));
+  if (!anybad) {
+    const int dsl = D / C;
+    for (int i = threadIdx.x; i < ng * dsl; i += threads) {
+      const int hh = i / dsl, d = r * dsl + (i - hh * dsl);
+      float M = -INFINITY;
+      for (int j = 0; j < C; ++j) M = fmaxf(M, ld_dsmem_f32x2(dsmem_addr(cmd + hh, j)).x);
+      float num = 0.f, den = 0.f;
+      for (int j = 0; j < C; ++j) {
+        const float2 md = ld_dsmem_f32x2(dsmem_addr(cmd + hh, j));
+        const float w = md.x == -INFINITY ? 0.f : ex2(md.x - M);
+        den += w * md.y;
+        num += w * ld_dsmem_f32(dsmem_addr(cs + hh * cs_stride + d, j));
+      }
+      OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + hh) * p.out_hs + d;
+      *o = static_cast<OutT>(den > 0.f ? num / den * vs : 0.f);
+    }
+  }
+  cluster_sync();
+}
+
 // Longest-first order of sequences (for batches of at most kLptMax sequences).
 // The block scheduler starts CTAs in increasing blockIdx order, so when CTA row z
 // works on the z-th longest sequence, the long sequences start first and the last

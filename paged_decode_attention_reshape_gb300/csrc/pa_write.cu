@@ -163,6 +163,11 @@ cudaError_t launch_one(const WriteParams &p, int sm_count, cudaStream_t st) {
   const int64_t cap = static_cast<int64_t>(sm_count) * 8;  // 8 x 256 threads per SM, grid-stride
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  // the write uses no shared memory and reads around L1; keep the SM's shared/L1 split the
+  // decode kernels ask for, so the usual write -> decode sequence does not reconfigure it
+  cudaError_t e = cudaFuncSetAttribute(write_kernel<DT, FP8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   write_kernel<DT, FP8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
   return cudaGetLastError();
 }

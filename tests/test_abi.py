@@ -138,9 +138,17 @@ def test_partition_plan_rules(L):
     assert pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, -1) == (0, 1)
     assert pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, 500) == (512, 256)
     assert pa.pa_decode_plan(4, 32, 8, 128, 8, pa.PA_BF16, 152, 512) == (0, 1)
-    # heuristic: a few long sequences are split, never below 1024 tokens per partition
+    # -2 / -4 / -8: cluster split into that many equal parts; other negative values are invalid
+    for C in (2, 4, 8):
+        assert pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, -C) == (-C, C)
+    for bad in (-3, -5, -16):
+        with pytest.raises(pa.PAError):
+            pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, bad)
+    # heuristic: a few long sequences get fixed partitions, never below 1024 tokens
     P, n = pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, 0)
-    assert P >= 1024 and P % 16 == 0 and n == -(-8192 * 16 // P) and n > 1
+    assert P >= 1024 and P % 16 == 0 and n == -(-8192 * 16 // P) and n > 8
+    # heuristic: a batch that fits the resident slots gets its longest sequences cut in two
+    assert pa.pa_decode_plan(64, 32, 8, 64, 128, pa.PA_BF16, 152, 0) == (1024, 2)
     # heuristic: a partition as long as the table is no split
     assert pa.pa_decode_plan(64, 32, 8, 64, 64, pa.PA_BF16, 152, 0) == (0, 1)
     # heuristic: a longest-first batch whose units fill the resident slots is not split
@@ -156,6 +164,7 @@ def test_workspace_size(L):
     S, Hq, Hkv, D, MB = 4, 32, 8, 128, 8192
     assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, MB, 0) == 0
     assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, MB, -1) == 0
+    assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, MB, -4) == 0           # cluster split: no workspace
     assert pa.pa_decode_workspace_size(S, 30, Hkv, D, MB, 512) == 0           # Hq % Hkv != 0
     parts = -(-MB * 16 // 512)
     rows = S * Hq * parts

@@ -13,7 +13,8 @@ import paged_decode_attention_reshape_gb300 as pa
 pytestmark = pytest.mark.gpu
 
 LENS = [0, 1, 15, 16, 17, 33, 100, 257, 700, 1100]   # empty, single token, ragged tails, several tiles
-PARTS = [-1, 16, 64, 512, 0]                          # unsplit, splits of 1/4/32 pages, heuristic
+PARTS = [-1, 16, 64, 512, 0, -2, -4, -8]              # unsplit, splits of 1/4/32 pages, heuristic,
+                                                      # cluster splits into 2/4/8 equal parts
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -73,14 +74,14 @@ def test_physical_permutation_does_not_change_the_result():
         perm = torch.randperm(nb, generator=torch.Generator().manual_seed(100 + perm_seed))
         c = make_case(4, 32, 8, 128, lens, seed=5, perm=perm)
         g = to_gpu(c)
-        outs.append([run(c, g, P).clone().cpu() for P in (-1, 64)])
+        outs.append([run(c, g, P).clone().cpu() for P in (-1, 64, -4)])
     for o in outs[1:]:
-        assert torch.equal(o[0], outs[0][0]) and torch.equal(o[1], outs[0][1])
+        assert all(torch.equal(a, b) for a, b in zip(o, outs[0]))
 
 
 def test_in_place_output_over_q():
     lens = [5, 100, 333]
-    for P in (-1, 32):
+    for P in (-1, 32, -4):
         c = make_case(3, 16, 4, 128, lens, seed=11)
         g = to_gpu(c)
         ref_out = run(c, g, P).clone()
@@ -118,7 +119,7 @@ def test_block_id_out_of_range_is_reported_not_faulted():
     c.block_table[1, 2] = c.NB + 7        # inside the sequence's first ceil(64/16) = 4 blocks
     c.block_table[2, 0] = -3
     g = to_gpu(c)
-    for P in (-1, 16):
+    for P in (-1, 16, -2):
         run(c, g, P)
         rc, bits = pa.pa_check_device_error(g.err)
         assert rc == -6, (rc, bits)
