@@ -61,9 +61,12 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&x)[16 / In<DT>::
 struct Divisor {
   float s, y;
   bool fast;
-  __device__ __forceinline__ float div(float x) const {
+  __device__ __forceinline__ static bool in_range(float x) {
     const float ax = fabsf(x);
-    if (fast && ax >= 0x1p-80f && ax <= 0x1p80f) {  // false for NaN
+    return ax >= 0x1p-80f && ax <= 0x1p80f;  // false for zero, subnormals, inf, NaN
+  }
+  __device__ __forceinline__ float div(float x) const {
+    if (fast && in_range(x)) {
       float q = __fmul_rn(x, y);
       float r = __fmaf_rn(-q, s, x);
       q = __fmaf_rn(r, y, q);
@@ -71,6 +74,23 @@ struct Divisor {
       return __fmaf_rn(r, y, q);
     }
     return __fdiv_rn(x, s);
+  }
+  // The same correctly rounded steps on two operands at once (packed fp32x2 operations,
+  // each lane an IEEE round-to-nearest multiply / fused multiply-add); the caller has
+  // checked fast and in_range for both.
+  __device__ __forceinline__ float2 div2_fast(float a, float b) const {
+    uint64_t x, sy, ns, q, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(sy) : "f"(y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ns) : "f"(-s));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(x), "l"(sy));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q), "l"(ns), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(q) : "l"(r), "l"(sy));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q), "l"(ns), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(q) : "l"(r), "l"(sy));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(q));
+    return o;
   }
 };
 
@@ -83,25 +103,39 @@ __device__ __forceinline__ Divisor make_divisor(float s) {
   return d;
 }
 
-// E4M3 code pair of (a / s, b / s): correctly rounded fp32 quotient, then
-// round-to-nearest-even with saturation (cvt ... satfinite); low byte = a.
-__device__ __forceinline__ uint32_t quant2(float a, float b, const Divisor &dv) {
-  const float2 y = make_float2(dv.div(a), dv.div(b));
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3));
+// E4M3 code pair of two quotients (cvt ... satfinite: round-to-nearest-even with
+// saturation); low byte = a.
+__device__ __forceinline__ uint32_t e4m3_pair(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
+// One 16-byte pack of inputs -> E4M3 codes of x / scale (correctly rounded quotient).
 template <int DT>
 __device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, const Divisor &dv) {
   constexpr int E = 16 / In<DT>::bytes;
-  float x[E];
+  float x[E], q[E];
   unpack8<DT>(v, x);
+  bool fast = dv.fast;
+#pragma unroll
+  for (int i = 0; i < E; ++i) fast &= Divisor::in_range(x[i]);
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const float2 r = dv.div2_fast(x[i], x[i + 1]);
+      q[i] = r.x;
+      q[i + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) q[i] = dv.div(x[i]);
+  }
   if constexpr (E == 8) {
     uint2 o;
-    o.x = quant2(x[0], x[1], dv) | (quant2(x[2], x[3], dv) << 16);
-    o.y = quant2(x[4], x[5], dv) | (quant2(x[6], x[7], dv) << 16);
+    o.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
+    o.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
     *reinterpret_cast<uint2 *>(dst) = o;
   } else {
-    *reinterpret_cast<uint32_t *>(dst) = quant2(x[0], x[1], dv) | (quant2(x[2], x[3], dv) << 16);
+    *reinterpret_cast<uint32_t *>(dst) = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
   }
 }
 
