@@ -272,23 +272,40 @@ def time_steps(st, K, flush, partition_size, ws, profile=False):
     return [a.elapsed_time(b) for a, b in ev], prof
 
 
+E2E_INPUTS = ("q", "k_step", "v_step", "slot_mapping", "block_table", "seq_lens")
+
+
 def e2e_steps(st, K, flush, partition_size, ws):
-    """Same step fed from pinned host buffers: H2D of the step's inputs (q, new K/V rows,
-    slot_mapping, block_table, seq_lens) and D2H of the output inside the timed events."""
-    host = {name: getattr(st, name).cpu().pin_memory() for name in
-            ("q", "k_step", "v_step", "slot_mapping", "block_table", "seq_lens")}
+    """Same step fed from host memory: the step's inputs (q, new K/V rows, slot_mapping,
+    block_table, seq_lens) sit packed in one pinned host buffer, are copied to one device
+    staging buffer (one H2D copy), the library runs on views of it, and the output comes
+    back with one D2H copy, all inside the timed events."""
+    import copy
+    names = E2E_INPUTS
+    offs, off = {}, 0
+    for n in names:
+        t = getattr(st, n)
+        offs[n] = off
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(off, dtype=torch.uint8, device=st.q.device)
+    view = copy.copy(st)
+    for n in names:
+        t = getattr(st, n)
+        nb = t.numel() * t.element_size()
+        host[offs[n]:offs[n] + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+        setattr(view, n, dev[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape))
     out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = off
     d2h = out_h.numel() * out_h.element_size()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize()
     for i in range(K):
         flush()
         ev[i][0].record()
-        for name, t in host.items():
-            getattr(st, name).copy_(t, non_blocking=True)
-        run_step(st, partition_size, ws)
-        out_h.copy_(st.out, non_blocking=True)
+        dev.copy_(host, non_blocking=True)
+        run_step(view, partition_size, ws)
+        out_h.copy_(view.out, non_blocking=True)
         ev[i][1].record()
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in ev], h2d, d2h
@@ -324,7 +341,8 @@ def cpu_baseline(w, target_s=12.0, max_seqs=None):
         oracle.dense_decode(qs[s], K, V, w.scale)
         return L
 
-    # calibrate on one sequence, then size the sample to about target_s of wall time
+    # calibrate on one sequence, then size the sample to about target_s of wall time; a
+    # workload the host finishes faster than that is run in repeated passes
     first = int(order[0])
     t = time.perf_counter()
     item0 = (first, prep(first))
@@ -335,29 +353,38 @@ def cpu_baseline(w, target_s=12.0, max_seqs=None):
         n = min(n, max_seqs)
     sample = [int(x) for x in order[:n]]
     items = [(s, prep(s)) for s in sample]
+    passes = 0
     t = time.perf_counter()
     with ThreadPoolExecutor(max_workers=cores) as ex:
-        list(ex.map(work, items))
+        while True:
+            list(ex.map(work, items))
+            passes += 1
+            if time.perf_counter() - t >= target_s:
+                break
     dt = time.perf_counter() - t
     nb = sum((int(w.seq_lens[s]) + 15) // 16 for s in sample)
     bytes_ = nb * 16 * w.Hkv * w.D * w.cache_elem_bytes() * 2 + 2 * n * w.Hq * w.D * w.in_elem_bytes() + nb * 4 + n * 4
-    return {"value": bytes_ / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": "%d of %d sequences (all %d query heads, fp64 dense decode%s), %.2f s"
-                      % (n, w.S, w.Hq, " + e4m3 quantisation" if w.kv_dtype == "e4m3" else "", dt),
-            "tokens_per_s": n / dt}
+    return {"value": passes * bytes_ / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d pass(es) over %d of %d sequences (all %d query heads, fp64 dense decode%s), %.2f s"
+                      % (passes, n, w.S, w.Hq, " + e4m3 quantisation" if w.kv_dtype == "e4m3" else "", dt),
+            "tokens_per_s": passes * n / dt}
 
 
 # --------------------------------------------------------------------- main
 
-def dist_setup():
+def dist_setup(backend: str = "nccl"):
+    """Rank layout from the torchrun environment.  Every rank works on its own GPU and its
+    own batch (the path shards by sequence with no exchange), so the process group only
+    carries the barrier and the max-over-ranks timing."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return ws, rank, local
 
@@ -368,13 +395,18 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(x, ws):
+def max_over_ranks(x, ws, device="cuda"):
     if ws <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(bytes_per_rank: int, ws: int, ms_max: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time."""
+    return ws * bytes_per_rank / (ms_max * 1e-3) / 1e9
 
 
 def main_reference(args):
@@ -481,7 +513,7 @@ def main(argv=None):
     ms = float(np.mean(step_ms))
     ms = max_over_ranks(ms, ws)
     dec_bytes = w.decode_bytes()
-    value = ws * dec_bytes / (ms * 1e-3) / 1e9
+    value = job_throughput(dec_bytes, ws, ms)
     wr_ms, wr_n = prof[pa.PA_KERNEL_WRITE]
     dk_ms, dk_n = prof[pa.PA_KERNEL_DECODE]
     dk_avg = dk_ms / max(1, dk_n)
@@ -493,7 +525,7 @@ def main(argv=None):
     if not args.no_e2e:
         e_ms, h2d, d2h = e2e_steps(st, max(10, min(args.steps, 200)), flush, args.partition_size, wspace)
         em = max_over_ranks(float(np.mean(e_ms)), ws)
-        e2e = {"value": ws * dec_bytes / (em * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(dec_bytes, ws, em), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": em}
 
     cpu = None
