@@ -126,7 +126,8 @@ def workspace_for(st: Staged, partition_size: int):
     w = st.w
     code = {"f32": pa.PA_F32, "bf16": pa.PA_BF16, "e4m3": pa.PA_FP8_E4M3}[w.cache_dtype]
     P, nparts = pa.pa_decode_plan(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, code, 0, partition_size)
-    nbytes = pa.pa_decode_workspace_size(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, P) if P > 0 else 0
+    nbytes = pa.pa_decode_workspace_size(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, P) \
+        if (P > 0 or P == pa.PA_PARTITION_BALANCED) else 0
     ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=st.q.device)   # zero before first use
     return P, nparts, ws
 

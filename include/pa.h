@@ -164,7 +164,12 @@ int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, cons
  *                     16), merged through the workspace; -2, -4 or -8 = every sequence
  *                     cut into 2, 4 or 8 equal parts processed by the CTAs of one
  *                     thread-block cluster and merged through distributed shared
- *                     memory (no workspace).
+ *                     memory (no workspace); PA_PARTITION_BALANCED = the balanced
+ *                     split: the pages of all sequences, concatenated, cut into equal
+ *                     ranges over one resident wave of CTAs per (kv head, head group),
+ *                     the parts of a cut sequence merged through the workspace
+ *                     (batches of at most 511 sequences, else
+ *                     PA_ERR_UNSUPPORTED_SHAPE; the fp32 cache runs it unsplit).
  *   workspace,        device memory for split-KV partition states; at least
  *   workspace_bytes   pa_decode_workspace_size(...) bytes for the partition size
  *                     the call ends up using (0 bytes when it does not split or
@@ -181,6 +186,7 @@ int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, cons
  * programmatic dependent of the preceding work on `stream` and waits for it before
  * reading any input.
  */
+#define PA_PARTITION_BALANCED (-100)
 int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                  const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
                  const float *k_scale, const float *v_scale, int partition_size, void *workspace,
@@ -222,9 +228,12 @@ int pa_decode_noalloc(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cac
  * pa_decode_plan -- host-only: the split pa_decode_ex would use.
  *   kv_dtype_code   pa_dtype of the cache; sm_count <= 0 queries the current device.
  *   partition_size  in: as for pa_decode_ex.  *partition_out: tokens per fixed
- *                   partition, 0 = unsplit, or -C for the cluster split into C parts;
- *                   *num_partitions_out: partitions of the longest possible sequence
- *                   (max_blocks_per_seq * 16 tokens), or C.
+ *                   partition, 0 = unsplit, -C for the cluster split into C parts, or
+ *                   PA_PARTITION_BALANCED; *num_partitions_out: partitions of the
+ *                   longest possible sequence (max_blocks_per_seq * 16 tokens), C, or
+ *                   the balanced split's CTAs per (kv head, head group).
+ *                   With sm_count > 0 the CTAs resident per SM are the shared-memory
+ *                   bound; with sm_count <= 0, the current device's occupancy.
  * Returns PA_OK or PA_ERR_INVALID_ARG.  No device memory is touched.
  */
 int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_blocks_per_seq,
@@ -234,7 +243,8 @@ int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
 /*
  * pa_decode_workspace_size -- bytes of split-KV workspace for `partition_size`
  * tokens per partition (0 or -1 = unsplit -> 0 bytes; invalid arguments -> 0).
- * Host-only.
+ * For PA_PARTITION_BALANCED: enough for any cache type on the current device
+ * (0 when no device can be queried).  Host-only.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                                 int max_blocks_per_seq, int partition_size);

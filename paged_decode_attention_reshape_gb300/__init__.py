@@ -33,6 +33,7 @@ EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_ex", "pa_decode_noall
            "pa_decode_workspace_size", "pa_check_device_error", "pa_status_string", "pa_profile_enable",
            "pa_profile_read")
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
+PA_PARTITION_BALANCED = -100  # partition_size: balanced split over one resident wave
 
 _DT = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16, torch.uint8: PA_FP8_E4M3,
        torch.int32: PA_I32, torch.int64: PA_I64}

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -150,8 +151,22 @@ int kind_of(int q_dtype, int cache_dtype) {
 // Batches the tensor-core kernel runs longest-first (see lpt_sequence).
 bool longest_first(int kind, int S) { return kind != KIND_F32 && S <= 128; }
 
-int ctas_per_sm(int kind, int D) {
+// Resident CTAs per SM of the decode kernel for (kind, D).  With `device`, the CUDA
+// occupancy calculator's answer for the current device (cached per shape); otherwise,
+// or when that query fails, the shared-memory bound alone (a what-if plan for another
+// GPU, or a host without one).
+int ctas_per_sm(int kind, int D, bool device) {
   if (kind == KIND_F32) return 4;
+  if (device) {
+    static std::atomic<int> cache[5][3];
+    const int di = D == 64 ? 0 : D == 128 ? 1 : 2;
+    int n = cache[kind][di].load(std::memory_order_relaxed);
+    if (n == 0) {
+      n = (kind == KIND_BF16 || kind == KIND_F16) ? occupancy_decode_mma_16(kind, D) : occupancy_decode_mma_fp8(kind, D);
+      if (n > 0) cache[kind][di].store(n, std::memory_order_relaxed);
+    }
+    if (n > 0) return n;
+  }
   const size_t smem = mma_smem(kind, D);
   int n = static_cast<int>((227u * 1024u) / (smem + 1024));
   return std::max(1, std::min(n, 16));
@@ -171,7 +186,7 @@ int ctas_per_sm(int kind, int D) {
 // Fitted on GB300 to sweeps over partition sizes for the benchmark workloads:
 // 128 x 1k..8k tokens and 256 x 512..4096 run best unsplit, 64 x 1..2048 with its
 // longest sequences cut in two (1024), 4 x 32k..128k near 2048 tokens.
-int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, int request) {
+int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, bool device, int request) {
   if (request < 0) return 0;
   const int max_tokens = maxNB * kBlock;
   int P;
@@ -180,7 +195,7 @@ int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, i
   } else {
     const int G = Hq / Hkv;
     const int64_t units = static_cast<int64_t>(S) * Hkv * ((G + 7) / 8);
-    const int64_t slots = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D);
+    const int64_t slots = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D, device);
     if ((longest_first(kind, S) && units >= slots) || units >= 2 * slots) return 0;
     const int64_t work = units * std::max(1, maxNB / 2);  // pages, assuming half-full tables
     const int64_t pages = std::max<int64_t>(work / (2 * slots), 64);
@@ -192,43 +207,58 @@ int plan_partition(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, i
 }
 
 // The full plan: fixed-size partitions (P tokens, merged through the workspace by the
-// last-arriving CTA) or, on request only (request = -2, -4 or -8), a cluster split:
-// each unit cut into C equal parts whose CTAs form one thread-block cluster and merge
-// through distributed shared memory, with no workspace.  The heuristic does not pick
-// the cluster split: cutting every unit (short ones too) multiplies the CTAs beyond the
-// resident slots, and on GB300 that cost more than the shorter critical path saved
-// (64 x 1..2048 tokens: 33.2 us unsplit, 34.3 / 42.1 / 56.1 us for C = 2 / 4 / 8,
-// 32.9 us with 1024-token partitions).
+// last-arriving CTA), the balanced split (request PA_PARTITION_BALANCED: one resident
+// wave of CTAs per head row, each taking an equal share of the batch's pages), or, on
+// request only (-2, -4 or -8), a cluster split: each unit cut into C equal parts whose
+// CTAs form one thread-block cluster and merge through distributed shared memory, with
+// no workspace.  The heuristic does not pick the cluster split: cutting every unit
+// (short ones too) multiplies the CTAs beyond the resident slots, and on GB300 that
+// cost more than the shorter critical path saved (64 x 1..2048 tokens: 33.2 us
+// unsplit, 34.3 / 42.1 / 56.1 us for C = 2 / 4 / 8, 32.9 us with 1024-token partitions).
 struct Plan {
   int P;        // tokens per fixed partition (0 = none)
   int cluster;  // parts per unit of the cluster split (0 = none)
+  int flat;     // CTAs per head row of the balanced split (0 = none)
   int status;
 };
-Plan make_plan(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, int request) {
-  Plan pl{0, 0, PA_OK};
+int balanced_ctas(int Hq, int Hkv, int D, int kind, int sm, bool device) {
+  const int64_t rows = static_cast<int64_t>(Hkv) * ((Hq / Hkv + 7) / 8);
+  const int64_t slots = static_cast<int64_t>(std::max(sm, 1)) * ctas_per_sm(kind, D, device);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(slots / rows, 65535)));
+}
+Plan make_plan(int S, int Hq, int Hkv, int D, int maxNB, int kind, int sm, bool device, int request) {
+  Plan pl{0, 0, 0, PA_OK};
+  if (request == PA_PARTITION_BALANCED) {
+    if (kind == KIND_F32) return pl;  // the CUDA-core kernel runs it unsplit
+    if (S > kFlatMaxSeqs) pl.status = PA_ERR_UNSUPPORTED_SHAPE;
+    else pl.flat = balanced_ctas(Hq, Hkv, D, kind, sm, device);
+    return pl;
+  }
   if (request <= -2) {
     const int C = -request;
     if (C != 2 && C != 4 && C != 8) pl.status = PA_ERR_INVALID_ARG;
     else pl.cluster = C;
     return pl;
   }
-  pl.P = plan_partition(S, Hq, Hkv, D, maxNB, kind, sm, request);
+  pl.P = plan_partition(S, Hq, Hkv, D, maxNB, kind, sm, device, request);
   return pl;
 }
 
 // Split-KV workspace: [arrival counters, one int per (sequence, kv head, head group)]
-// [partition (m, l): float2 per (sequence, head, partition)] [partition acc: D floats each],
-// each region starting on a 256-byte boundary.
+// [partial (m, l): one float2 per row] [partial acc: D floats per row], each region
+// starting on a 256-byte boundary.  Rows: one per (sequence, head, partition) for
+// fixed-size partitions; 2 x 8 per CTA for the balanced split (`flat` CTAs per head row).
 struct WsLayout {
   size_t ml_off, acc_off, total;
 };
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-WsLayout workspace_layout(int S, int Hq, int Hkv, int D, int maxNB, int P) {
+WsLayout workspace_layout(int S, int Hq, int Hkv, int D, int maxNB, int P, int flat) {
   WsLayout L{0, 0, 0};
-  if (P <= 0) return L;
-  const int64_t parts = (static_cast<int64_t>(maxNB) * kBlock + P - 1) / P;
-  const int64_t rows = static_cast<int64_t>(S) * Hq * parts;
-  const int64_t units = static_cast<int64_t>(S) * Hkv * ((Hq / Hkv + 7) / 8);
+  if (P <= 0 && flat <= 0) return L;
+  const int64_t head_rows = static_cast<int64_t>(Hkv) * ((Hq / Hkv + 7) / 8);
+  const int64_t rows = flat > 0 ? head_rows * flat * 16
+                                : static_cast<int64_t>(S) * Hq * ((static_cast<int64_t>(maxNB) * kBlock + P - 1) / P);
+  const int64_t units = static_cast<int64_t>(S) * head_rows;
   L.ml_off = round256(static_cast<size_t>(units) * sizeof(int));
   L.acc_off = L.ml_off + round256(static_cast<size_t>(rows) * sizeof(float2));
   L.total = L.acc_off + static_cast<size_t>(rows) * D * sizeof(float);
@@ -367,14 +397,18 @@ PA_API int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int hea
     case PA_F32: kind = KIND_F32; break;
     default: return PA_ERR_INVALID_ARG;
   }
-  if (sm_count <= 0) sm_count = device_sm_count();
+  const bool device = sm_count <= 0;
+  if (device) sm_count = device_sm_count();
   if (sm_count <= 0) return PA_ERR_CUDA;
-  const Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kind, sm_count,
+  const Plan pl = make_plan(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, kind, sm_count, device,
                             partition_size);
   if (pl.status != PA_OK) return pl.status;
-  if (partition_out) *partition_out = pl.cluster > 1 ? -pl.cluster : pl.P;
+  if (partition_out) *partition_out = pl.flat > 0 ? PA_PARTITION_BALANCED : pl.cluster > 1 ? -pl.cluster : pl.P;
   if (num_partitions_out)
-    *num_partitions_out = pl.cluster > 1 ? pl.cluster : pl.P > 0 ? (max_blocks_per_seq * kBlock + pl.P - 1) / pl.P : 1;
+    *num_partitions_out = pl.flat > 0       ? pl.flat
+                          : pl.cluster > 1 ? pl.cluster
+                          : pl.P > 0       ? (max_blocks_per_seq * kBlock + pl.P - 1) / pl.P
+                                           : 1;
   return PA_OK;
 }
 
@@ -383,9 +417,18 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size < 0 ||
       max_blocks_per_seq < 0)
     return 0;
+  if (partition_size == PA_PARTITION_BALANCED) {
+    // enough for any cache type on the current device: the E4M3 kernel's shared-memory
+    // bound admits the most CTAs per SM
+    const int sm = device_sm_count();
+    if (sm <= 0 || num_seqs > kFlatMaxSeqs) return 0;
+    const int kind = head_size >= 128 ? KIND_FP8_BF16Q : KIND_BF16;
+    const int flat = balanced_ctas(num_heads, num_kv_heads, head_size, kind, sm, false);
+    return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, 0, flat).total;
+  }
   const int P = partition_size > 0 ? (partition_size + kBlock - 1) / kBlock * kBlock : 0;
   if (P >= max_blocks_per_seq * kBlock) return 0;
-  return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, P).total;
+  return workspace_layout(num_seqs, num_heads, num_kv_heads, head_size, max_blocks_per_seq, P, 0).total;
 }
 
 namespace {
@@ -426,7 +469,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   const int maxNB = static_cast<int>(block_table->shape[1]);
   const int sm = device_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
-  const Plan pl = make_plan(S, Hq, Hkv, D, maxNB, kind, sm, partition_size);
+  const Plan pl = make_plan(S, Hq, Hkv, D, maxNB, kind, sm, true, partition_size);
   if (pl.status != PA_OK) return pl.status;
   const int P = pl.P;
   const int max_parts = pl.cluster > 1 ? pl.cluster : P > 0 ? (maxNB * kBlock + P - 1) / P : 1;
@@ -456,19 +499,22 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   p.pages_per_part = P > 0 ? P / kBlock : std::max(maxNB, 1);
   p.max_parts = max_parts;
   p.cluster = pl.cluster;
+  p.flat = pl.flat;
   p.err = device_error;
   {
     // Order the batch longest-first only when its CTAs cannot all be resident at once:
     // with every CTA resident from the start the order buys nothing and the ranking
     // (a read of every length plus two block barriers) sits on each CTA's critical path.
     const int64_t ctas = static_cast<int64_t>(S) * Hkv * p.HG * max_parts;
-    p.lpt = (longest_first(kind, S) && ctas > static_cast<int64_t>(sm) * ctas_per_sm(kind, D)) ? 1 : 0;
+    p.lpt = (pl.flat == 0 && longest_first(kind, S) && ctas > static_cast<int64_t>(sm) * ctas_per_sm(kind, D, true))
+                ? 1
+                : 0;
   }
   if (kind != KIND_FP8_BF16Q && kind != KIND_FP8_F16Q) p.k_scale = p.v_scale = nullptr;
   if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
 
-  if (max_parts > 1 && pl.cluster <= 1) {
-    const WsLayout lay = workspace_layout(S, Hq, Hkv, D, maxNB, P);
+  if ((max_parts > 1 && pl.cluster <= 1) || pl.flat > 0) {
+    const WsLayout lay = workspace_layout(S, Hq, Hkv, D, maxNB, P, pl.flat);
     if (internal_ws) {
       int dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
   static_assert(sizeof(sm) >= 8 * kMergeSmemParts * 4, "merge weights reuse sm");
   if (!direct)
     merge_if_last<float, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, 1.f, W * 32,
-                            &sm[0][0][0]);
+                            &sm[0][0][0], FixedRows{static_cast<int64_t>(s) * p.Hq + h0, p.max_parts});
 }
 
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st) {

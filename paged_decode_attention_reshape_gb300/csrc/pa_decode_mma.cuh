@@ -76,102 +76,34 @@ struct MmaCfg {
   static_assert(STAGES * STAGEB >= 64 + 8 * D * 4, "warp region must hold the merge state");
   static_assert(static_cast<size_t>(W) * STAGES * STAGEB >= 8 * kMergeSmemParts * 4, "merge weights");
   static_assert(kMmaScratch >= kLptScratchBytes, "ranking scratch");
+  static_assert(kMmaScratch >= (kFlatMaxSeqs + 1) * 4, "balanced-split page offsets");
 };
 
+// Runs pages [pb, pe) of sequence s (length len) for KV head g and the query heads
+// h0 .. h0+ng-1 through the warps' pipelines, and leaves each warp's state at the
+// start of its own stage region: (m, l) per head, then acc[8][D].  `used` counts the
+// pages this warp has already taken through its stages: the mbarrier phases go on
+// from there, so a CTA can run several ranges in a row.  With `pid_ready`, pid_reg
+// already holds lane i's table entry for the warp's i-th page (read early by the
+// caller).  Returns true after a bad block id or a timed-out wait; `stalled` is set
+// on a timeout, after which the CTA must not issue into its stages again.
 template <int KIND, int D, int W, int STAGES>
-__global__ void __launch_bounds__(W * 32)
-    decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+__device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                          const uint32_t sbase, uint8_t *const sgen, int &used, bool &stalled,
+                                          const int s, const int len, const int g, const int h0, const int ng,
+                                          const int pb, const int pe, int pid_reg, const bool pid_ready,
+                                          const uint64_t pol) {
   using C = MmaCfg<KIND, D, W, STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_u32 = smem_u32(smem_raw);
-  const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;  // 128B-swizzle boxes need 1 KiB alignment
-  uint8_t *const sgen = smem_raw + (sbase - raw_u32);
-
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int part = blockIdx.x;
-  const int g = blockIdx.y / p.HG, hg = blockIdx.y - g * p.HG;
-  const int h0 = g * p.G + hg * 8;      // first query head of this CTA
-  const int ng = min(8, p.G - hg * 8);  // query heads in the group
-  const bool split = p.max_parts > 1;
-  using OutT = typename std::conditional<C::QBF16, __nv_bfloat16, __half>::type;
-
-  // Warm L2 with the metadata this launch reads on its critical path: CTA row z
-  // prefetches sequence z's slice of the block table (the first head group only) and
-  // its query heads (the first partition only); together the rows cover every
-  // sequence, whichever row ends up working on it.  A prefetch returns no data, so it
-  // may run before the wait on the previous grid.
-  if (warp == 0) {
-    const int z = blockIdx.z;
-    if (blockIdx.y == 0) {
-      const int pg0 = p.cluster > 1 ? part * p.max_blocks / p.cluster : part * p.pages_per_part;
-      const int pg1 = p.cluster > 1 ? (part + 1) * p.max_blocks / p.cluster : min(p.max_blocks, pg0 + p.pages_per_part);
-      const int32_t *row = p.block_table + static_cast<int64_t>(z) * p.bt_ss;
-      for (int pg = pg0 + lane * 32; pg < pg1; pg += 32 * 32) prefetch_l2(row + pg);
-    }
-    if (part == 0) {
-      const char *qr = static_cast<const char *>(p.q) +
-                       (static_cast<int64_t>(z) * p.q_ss + static_cast<int64_t>(h0) * p.q_hs) * 2;
-      const int bytes = ng * D * 2;
-      if (lane * 128 < bytes && p.q_hs == D) prefetch_l2(qr + lane * 128);
-    }
-  }
-  grid_dependency_wait();
-  const int s = p.lpt ? lpt_sequence(p.seq_lens, p.S, blockIdx.z, C::THREADS,
-                                    reinterpret_cast<int *>(sgen + C::SCRATCH_OFF))
-                      : static_cast<int>(blockIdx.z);
   const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
-  const int len = __ldg(p.seq_lens + s);
-  const bool clustered = p.cluster > 1;  // rank `part` of a cluster splitting the unit equally
-  int pid_reg = 0;  // lane i: physical block of my page (32 * chunk + i); with fixed-size
-                    // partitions chunk 0 is read speculatively (bounded by the table width)
-                    // alongside seq_len
-  if (!clustered) {
-    const int pg = part * p.pages_per_part + warp + lane * W;
-    if (pg < p.max_blocks) pid_reg = __ldg(bt + pg);
-  }
-  if (len < 0 || len > p.max_blocks * kBlock) {  // (all ranks of a cluster see the same length)
-    if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
-    return;
-  }
-  const int npages = (len + kBlock - 1) / kBlock;
-  int pb, pe;
-  if (clustered) {
-    pb = static_cast<int>(static_cast<int64_t>(part) * npages / p.cluster);
-    pe = static_cast<int>(static_cast<int64_t>(part + 1) * npages / p.cluster);
-    const int pg = pb + warp + lane * W;
-    if (pg < pe) pid_reg = __ldg(bt + pg);
-  } else {
-    pb = part * p.pages_per_part;
-    pe = min(npages, pb + p.pages_per_part);
-  }
-  if (pb >= pe && !clustered) {  // (an empty cluster rank stays: it takes part in the merge)
-    if (!split && part == 0) {  // empty sequence: zero output rows
-      for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
-        OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D;
-        *o = OutT(0.f);
-      }
-    }
-    return;
-  }
-
-  // ---------------------------------------------------------------- pipeline
   const int nmine = (pe - pb > warp) ? (pe - pb - warp + W - 1) / W : 0;
   const uint32_t stage0 = sbase + static_cast<uint32_t>(warp * STAGES * C::STAGEB);
   const uint32_t bar0 = sbase + static_cast<uint32_t>(W * STAGES * C::STAGEB + warp * STAGES * 8);
-  if (lane == 0) {
-    for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
-    fence_barrier_init();
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
-  __syncwarp();
-
-  const uint64_t pol = policy_evict_first();
+  const int u0 = used;
   bool bad = false;
 
   auto issue = [&](int kk) {  // whole warp; kk increases by one per call
-    if ((kk & 31) == 0 && kk > 0) {
+    if ((kk & 31) == 0 && (kk > 0 || !pid_ready)) {
       const int k2 = kk + lane;
       pid_reg = (k2 < nmine) ? __ldg(bt + pb + warp + k2 * W) : 0;
     }
@@ -182,15 +114,15 @@ __global__ void __launch_bounds__(W * 32)
       pid = 0;  // load a valid block; the CTA writes nothing
     }
     if (lane == 0) {
-      const int st = kk % STAGES;
+      const int st = (u0 + kk) % STAGES;
       const uint32_t bar = bar0 + 8 * st;
       const uint32_t kdst = stage0 + st * C::STAGEB;
       mbar_arrive_expect_tx(bar, C::STAGEB);
 #pragma unroll
-      for (int b = 0; b < C::NBOX; ++b) tma_load_4d(kdst + b * 2048, &tmK, bar, b * C::BOXE, 0, g, pid, pol);
+      for (int b = 0; b < C::NBOX; ++b) tma_load_4d(kdst + b * 2048, tmK, bar, b * C::BOXE, 0, g, pid, pol);
 #pragma unroll
       for (int b = 0; b < C::NBOX; ++b)
-        tma_load_4d(kdst + C::PAGEB + b * 2048, &tmV, bar, b * C::BOXE, 0, g, pid, pol);
+        tma_load_4d(kdst + C::PAGEB + b * 2048, tmV, bar, b * C::BOXE, 0, g, pid, pol);
     }
   };
 
@@ -262,6 +194,7 @@ __global__ void __launch_bounds__(W * 32)
     sc1 = p.scale_log2 * ks / sf1;
   }
 
+
   // --------------------------------------------------------------- main loop
   float acc[C::KT][4];
 #pragma unroll
@@ -270,12 +203,14 @@ __global__ void __launch_bounds__(W * 32)
   const int ra = lane >> 2;  // token row of score fragments (and +8)
 
   for (int k = 0; k < nmine; ++k) {
-    const int st = k % STAGES;
-    if (!mbar_wait_bounded(bar0 + 8 * st, (k / STAGES) & 1, kWaitLimit)) {
+    const int u = u0 + k;  // this page's use of the warp's stages
+    const int st = u % STAGES;
+    if (!mbar_wait_bounded(bar0 + 8 * st, (u / STAGES) & 1, kWaitLimit)) {
       bad = true;
+      stalled = true;
       if (lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
       for (int k2 = k + 1; k2 < min(nmine, k + STAGES); ++k2)  // drain copies in flight
-        mbar_wait_bounded(bar0 + 8 * (k2 % STAGES), (k2 / STAGES) & 1, kWaitLimit);
+        mbar_wait_bounded(bar0 + 8 * ((u0 + k2) % STAGES), ((u0 + k2) / STAGES) & 1, kWaitLimit);
       break;
     }
     const uint32_t kb = stage0 + st * C::STAGEB;
@@ -431,6 +366,7 @@ __global__ void __launch_bounds__(W * 32)
       issue(k + STAGES);
     }
   }
+  used = u0 + nmine;
 
   // ------------------------------------------------------ merge warp states
 #pragma unroll
@@ -458,9 +394,255 @@ __global__ void __launch_bounds__(W * 32)
       wacc[head * D + d] = acc[t][i];
     }
   }
+  return bad;
+}
+
+// Merges the W warp states of the CTA (max / log-sum-exp rescaling) and, for every
+// (head, element) of the group, writes the normalised output (direct) or stores the
+// CTA's state (m, l, unnormalised acc) in workspace row rows(hh).
+template <int KIND, int D, int W, int STAGES, typename OutT, typename RowFn>
+__device__ __forceinline__ void write_cta_state(const DecodeParams &p, const uint8_t *sgen, int s, int h0, int ng,
+                                                float vs, bool direct, RowFn rows) {
+  using C = MmaCfg<KIND, D, W, STAGES>;
+  for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
+    const int hh = i / D, d = i - hh * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
+      M = fmaxf(M, ml[2 * hh]);
+    }
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
+      const float mw = ml[2 * hh];
+      const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      den += sc * ml[2 * hh + 1];
+      num += sc * ml[16 + hh * D + d];
+    }
+    if (direct) {
+      OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + hh) * p.out_hs + d;
+      *o = OutT(den > 0.f ? num / den * vs : 0.f);
+    } else {
+      const int64_t r = rows(hh);
+      p.part_acc[r * D + d] = num;
+      if (d == 0) p.part_ml[r] = make_float2(M, den);
+    }
+  }
+}
+
+template <typename OutT>
+__device__ __forceinline__ void zero_rows(const DecodeParams &p, int s, int h0, int ng, int D, int threads) {
+  for (int i = threadIdx.x; i < ng * D; i += threads) {
+    OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D;
+    *o = OutT(0.f);
+  }
+}
+
+template <int KIND, int D, int W, int STAGES>
+__global__ void __launch_bounds__(W * 32)
+    decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+  using C = MmaCfg<KIND, D, W, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;  // 128B-swizzle boxes need 1 KiB alignment
+  uint8_t *const sgen = smem_raw + (sbase - raw_u32);
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int part = blockIdx.x;
+  const int g = blockIdx.y / p.HG, hg = blockIdx.y - g * p.HG;
+  const int h0 = g * p.G + hg * 8;      // first query head of this CTA
+  const int ng = min(8, p.G - hg * 8);  // query heads in the group
+  const bool flat = p.flat > 0;
+  using OutT = typename std::conditional<C::QBF16, __nv_bfloat16, __half>::type;
+
+  if (lane == 0) {  // this warp's stage barriers, before any memory operation (the init fence is a release)
+    const uint32_t bar0 = sbase + static_cast<uint32_t>(W * STAGES * C::STAGEB + warp * STAGES * 8);
+    for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncwarp();
+  // Warm L2 with the metadata this launch reads on its critical path.  A prefetch
+  // returns no data, so it may run before the wait on the previous grid.
+  if (warp == 0) {
+    if (lane == 0) prefetch_l2(p.seq_lens + (flat ? 0 : blockIdx.z));
+    if (flat) {  // CTA c: the table rows (first head row only) and query heads of sequences c, c + CTAs, ...
+      for (int z = part; z < p.S; z += p.flat) {
+        if (blockIdx.y == 0) {
+          const int32_t *row = p.block_table + static_cast<int64_t>(z) * p.bt_ss;
+          for (int pg = lane * 32; pg < p.max_blocks; pg += 32 * 32) prefetch_l2(row + pg);
+        }
+        const char *qr = static_cast<const char *>(p.q) +
+                         (static_cast<int64_t>(z) * p.q_ss + static_cast<int64_t>(h0) * p.q_hs) * 2;
+        if (lane * 128 < ng * D * 2 && p.q_hs == D) prefetch_l2(qr + lane * 128);
+      }
+    } else {
+      // CTA row z prefetches sequence z's slice of the block table (the first head group
+      // only) and its query heads (the first partition only); together the rows cover
+      // every sequence, whichever row ends up working on it.
+      const int z = blockIdx.z;
+      if (blockIdx.y == 0) {
+        const int pg0 = p.cluster > 1 ? part * p.max_blocks / p.cluster : part * p.pages_per_part;
+        const int pg1 = p.cluster > 1 ? (part + 1) * p.max_blocks / p.cluster : min(p.max_blocks, pg0 + p.pages_per_part);
+        const int32_t *row = p.block_table + static_cast<int64_t>(z) * p.bt_ss;
+        for (int pg = pg0 + lane * 32; pg < pg1; pg += 32 * 32) prefetch_l2(row + pg);
+      }
+      if (part == 0) {
+        const char *qr = static_cast<const char *>(p.q) +
+                         (static_cast<int64_t>(z) * p.q_ss + static_cast<int64_t>(h0) * p.q_hs) * 2;
+        if (lane * 128 < ng * D * 2 && p.q_hs == D) prefetch_l2(qr + lane * 128);
+      }
+    }
+  }
+  grid_dependency_wait();
+
+  const uint64_t pol = policy_evict_first();
+  const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.f;
+  float *const smem_w = reinterpret_cast<float *>(sgen);  // merge weights (stage buffers, free by then)
+  int used = 0;
+  bool stalled = false;
+
+  if (flat) {
+    // ----------------------------------------------------------- balanced split
+    // The pages of all sequences, concatenated in sequence order, are cut into
+    // p.flat equal ranges, one per CTA of this head row; a range may end inside one
+    // sequence and go on into the next.  A sequence held whole by one CTA is
+    // written directly; the parts of a cut sequence are merged by the last of its
+    // CTAs to finish.
+    int *pref = reinterpret_cast<int *>(sgen + C::SCRATCH_OFF);  // page offsets of the sequences [S + 1]
+    __shared__ int s_wsum[W];
+    {
+      constexpr int PER = (kFlatMaxSeqs + C::THREADS - 1) / C::THREADS;
+      const int i0 = threadIdx.x * PER;
+      int n[PER], sum = 0;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int i = i0 + j;
+        const int L = i < p.S ? __ldg(p.seq_lens + i) : 0;
+        const bool ok = L >= 0 && L <= p.max_blocks * kBlock;
+        if (!ok && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
+        n[j] = ok ? (L + kBlock - 1) / kBlock : 0;
+        sum += n[j];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) s_wsum[warp] = incl;
+      __syncthreads();
+      int run = incl - sum, total = 0;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const int v = s_wsum[w];
+        run += w < warp ? v : 0;
+        total += v;
+      }
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        if (i0 + j < p.S) pref[i0 + j] = run;
+        run += n[j];
+      }
+      if (threadIdx.x == 0) pref[p.S] = total;
+      __syncthreads();
+    }
+    for (int z = part; z < p.S; z += p.flat)  // empty sequences: zero output rows
+      if (pref[z] == pref[z + 1] && __ldg(p.seq_lens + z) == 0) zero_rows<OutT>(p, z, h0, ng, D, C::THREADS);
+
+    const int T = pref[p.S];
+    const int Ce = min(p.flat, T);  // CTAs with work: every range holds at least one page
+    if (part >= Ce) return;
+    const int a = static_cast<int>(static_cast<int64_t>(part) * T / Ce);
+    const int b = static_cast<int>(static_cast<int64_t>(part + 1) * T / Ce);
+    auto range_start = [&](int c) { return static_cast<int>(static_cast<int64_t>(c) * T / Ce); };
+    auto owner = [&](int x) { return static_cast<int>((static_cast<int64_t>(x + 1) * Ce - 1) / T); };
+    int z = 0;  // the sequence holding page a: the last z with pref[z] <= a (a non-empty one)
+    {
+      int hi = p.S - 1;
+      while (z < hi) {
+        const int mid = (z + hi + 1) >> 1;
+        if (pref[mid] <= a) z = mid;
+        else hi = mid - 1;
+      }
+    }
+    const int64_t my_row = static_cast<int64_t>(blockIdx.y) * p.flat + part;
+    bool dead = false;  // a wait timed out: no more copies into the stages
+    for (int x = a; x < b;) {
+      const int ps = pref[z], pn = pref[z + 1];
+      const int y = min(b, pn);
+      bool bad = true;
+      if (!dead)
+        bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, __ldg(p.seq_lens + z), g,
+                                            h0, ng, x - ps, y - ps, 0, false, pol);
+      const bool any_bad = __syncthreads_or(bad);
+      if (any_bad) dead = __syncthreads_or(stalled) || dead;
+      if (x == ps && y == pn) {
+        if (!any_bad) write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, z, h0, ng, vs, true, [](int) { return int64_t{0}; });
+      } else {
+        const int j = x == a ? 0 : 1;  // this CTA's first or last range
+        if (!any_bad)
+          write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, z, h0, ng, vs, false,
+                                                    [&](int hh) { return (my_row * 2 + j) * 8 + hh; });
+        // a CTA with an error still counts itself, so the unit's counter returns to zero
+        const int c0 = owner(ps);
+        merge_if_last<OutT, D>(p, z, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * z, h0, ng, owner(pn - 1) - c0 + 1,
+                               vs, C::THREADS, smem_w,
+                               FlatRows{static_cast<int64_t>(blockIdx.y) * p.flat + c0, range_start(c0) < ps ? 1 : 0});
+      }
+      x = y;
+      if (x < b) {
+        fence_proxy_async_smem();  // generic accesses to the stages before the next copies into them
+        __syncthreads();
+        do ++z;
+        while (pref[z + 1] == pref[z]);  // next non-empty sequence (one exists: x < b)
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------- one unit (or partition) per CTA
+  const int s = p.lpt ? lpt_sequence(p.seq_lens, p.S, blockIdx.z, C::THREADS,
+                                    reinterpret_cast<int *>(sgen + C::SCRATCH_OFF))
+                      : static_cast<int>(blockIdx.z);
+  const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
+  const int len = __ldg(p.seq_lens + s);
+  const bool clustered = p.cluster > 1;  // rank `part` of a cluster splitting the unit equally
+  const bool split = p.max_parts > 1;
+  int pid_reg = 0;  // lane i: physical block of my page i; with fixed-size partitions it is
+                    // read speculatively (bounded by the table width) alongside seq_len
+  if (!clustered) {
+    const int pg = part * p.pages_per_part + warp + lane * W;
+    if (pg < p.max_blocks) pid_reg = __ldg(bt + pg);
+  }
+  if (len < 0 || len > p.max_blocks * kBlock) {  // (all ranks of a cluster see the same length)
+    if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
+    return;
+  }
+  const int npages = (len + kBlock - 1) / kBlock;
+  int pb, pe;
+  if (clustered) {
+    pb = static_cast<int>(static_cast<int64_t>(part) * npages / p.cluster);
+    pe = static_cast<int>(static_cast<int64_t>(part + 1) * npages / p.cluster);
+    const int pg = pb + warp + lane * W;
+    if (pg < pe) pid_reg = __ldg(bt + pg);
+  } else {
+    pb = part * p.pages_per_part;
+    pe = min(npages, pb + p.pages_per_part);
+  }
+  if (pb >= pe && !clustered) {  // (an empty cluster rank stays: it takes part in the merge)
+    if (!split && part == 0) zero_rows<OutT>(p, s, h0, ng, D, C::THREADS);  // empty sequence
+    return;
+  }
+
+  const bool bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, g, h0, ng, pb,
+                                                 pe, pid_reg, true, pol);
   const bool any_bad = __syncthreads_or(bad);
 
-  const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.f;
   if (clustered) {
     // CTA state in place: element (hh, d) of warp 0's accumulator region is read only by
     // the thread that overwrites it; (max, exp-sum) per head go to the scratch area
@@ -491,39 +673,45 @@ __global__ void __launch_bounds__(W * 32)
   }
   const int nparts = split ? (npages + p.pages_per_part - 1) / p.pages_per_part : 1;
   const bool direct = nparts == 1;  // this CTA holds the whole sequence: write the output
-  if (!any_bad) {
-    for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
-      const int hh = i / D, d = i - hh * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
-        M = fmaxf(M, ml[2 * hh]);
-      }
-      float num = 0.f, den = 0.f;
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float *ml = reinterpret_cast<const float *>(sgen + w * STAGES * C::STAGEB);
-        const float mw = ml[2 * hh];
-        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        den += sc * ml[2 * hh + 1];
-        num += sc * ml[16 + hh * D + d];
-      }
-      const int h = h0 + hh;
-      if (direct) {
-        OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h) * p.out_hs + d;
-        *o = OutT(den > 0.f ? num / den * vs : 0.f);
-      } else {
-        const int64_t row = (static_cast<int64_t>(s) * p.Hq + h) * p.max_parts + part;
-        p.part_acc[row * D + d] = num;
-        if (d == 0) p.part_ml[row] = make_float2(M, den);
-      }
-    }
-  }
+  const FixedRows rows{static_cast<int64_t>(s) * p.Hq + h0, p.max_parts};
+  if (!any_bad)
+    write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, s, h0, ng, vs, direct, [&](int hh) { return rows(hh, part); });
   // a CTA with an error still counts itself, so the unit's counter returns to zero
   if (!direct)
     merge_if_last<OutT, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, vs, C::THREADS,
-                           reinterpret_cast<float *>(sgen));
+                           smem_w, rows);
 }
+
+// Host side of one (kind, head size) instantiation: function attributes, launch and
+// resident CTAs per SM.
+template <int KIND, int D>
+struct MmaLaunch {
+  static constexpr int W = mma_warps(KIND, D), ST = mma_stages(KIND, D);
+  using C = MmaCfg<KIND, D, W, ST>;
+  static_assert(C::SMEM == mma_smem(KIND, D), "shape table out of sync");
+
+  static cudaError_t attrs() {
+    auto kern = decode_mma_kernel<KIND, D, W, ST>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    // same shared/L1 split as the cache write that usually precedes it (no reconfiguration)
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  }
+  static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
+    cudaError_t e = attrs();
+    if (e != cudaSuccess) return e;
+    const dim3 grid = p.flat > 0 ? dim3(p.flat, p.Hkv * p.HG, 1) : dim3(p.max_parts, p.Hkv * p.HG, p.S);
+    e = launch_pdl(decode_mma_kernel<KIND, D, W, ST>, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p, tmK, tmV);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  static int occupancy() {  // 0 when it cannot be queried
+    int n = 0;
+    if (attrs() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<KIND, D, W, ST>, C::THREADS, C::SMEM) !=
+            cudaSuccess)
+      return 0;
+    return n;
+  }
+};
 
 }  // namespace pa

@@ -5,39 +5,33 @@
 namespace pa {
 namespace {
 
-template <int KIND, int D>
-cudaError_t go(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
-  constexpr int W = mma_warps(KIND, D), ST = mma_stages(KIND, D);
-  using C = MmaCfg<KIND, D, W, ST>;
-  static_assert(C::SMEM == mma_smem(KIND, D), "shape table out of sync");
-  auto kern = decode_mma_kernel<KIND, D, W, ST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
-  if (e != cudaSuccess) return e;
-  // same shared/L1 split as the cache write that usually precedes it (no reconfiguration)
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  const dim3 grid(p.max_parts, p.Hkv * p.HG, p.S);
-  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p, tmK, tmV);
-  return e != cudaSuccess ? e : cudaGetLastError();
+// f(MmaLaunch<kind, D>) for the instantiated shapes, else `other`.
+template <int KIND, typename R, typename F>
+R by_d(int D, R other, F f) {
+  switch (D) {
+    case 64: return f(MmaLaunch<KIND, 64>{});
+    case 128: return f(MmaLaunch<KIND, 128>{});
+    case 256: return f(MmaLaunch<KIND, 256>{});
+    default: return other;
+  }
 }
 
-template <int KIND>
-cudaError_t by_d(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
-  switch (p.D) {
-    case 64: return go<KIND, 64>(p, tmK, tmV, st);
-    case 128: return go<KIND, 128>(p, tmK, tmV, st);
-    case 256: return go<KIND, 256>(p, tmK, tmV, st);
-    default: return cudaErrorInvalidValue;
-  }
+template <typename R, typename F>
+R by_kind(int kind, int D, R other, F f) {
+  if (kind == KIND_BF16) return by_d<KIND_BF16>(D, other, f);
+  if (kind == KIND_F16) return by_d<KIND_F16>(D, other, f);
+  return other;
 }
 
 }  // namespace
 
 cudaError_t launch_decode_mma_16(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                  cudaStream_t st) {
-  if (kind == KIND_BF16) return by_d<KIND_BF16>(p, tmK, tmV, st);
-  if (kind == KIND_F16) return by_d<KIND_F16>(p, tmK, tmV, st);
-  return cudaErrorInvalidValue;
+  return by_kind(kind, p.D, cudaErrorInvalidValue, [&](auto L) { return decltype(L)::launch(p, tmK, tmV, st); });
+}
+
+int occupancy_decode_mma_16(int kind, int D) {
+  return by_kind(kind, D, 0, [](auto L) { return decltype(L)::occupancy(); });
 }
 
 }  // namespace pa

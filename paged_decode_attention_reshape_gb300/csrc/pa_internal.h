@@ -12,6 +12,7 @@
 namespace pa {
 
 constexpr int kBlock = PA_BLOCK_SIZE;  // tokens per KV-cache block (one "page")
+constexpr int kFlatMaxSeqs = 511;      // batch limit of the balanced split (page offsets kept in smem)
 
 // Cache element kinds of the decode kernels (query/output type in brackets).
 enum DecodeKind : int {
@@ -54,6 +55,7 @@ struct DecodeParams {
   float *part_acc;                     // [S, Hq, max_parts, D]
   int *err;                            // nullable
   int lpt;                             // 1: CTA row z takes the z-th longest sequence (S <= kLptMax)
+  int flat;                            // > 0: balanced split, this many CTAs per head row (S <= kFlatMaxSeqs)
   // fp32 path only: direct cache pointers and strides (elements)
   const float *kc, *vc;
   int64_t kc_s0, kc_s1, kc_s2, vc_s0, vc_s1, vc_s2;
@@ -70,11 +72,14 @@ cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, in
 
 // Tensor-core kernel shape per (kind, head size): warps per CTA and pipeline
 // stages per warp.  Shared memory = W * STAGES * 2 pages (+ alignment, barriers).
-constexpr int mma_warps(int kind, int D) { return (void)kind, (void)D, 4; }
-// Two stages per warp: pages of 2-8 KiB and 4 warps give 35-131 KiB per CTA, so 6
-// (2 KiB pages), 3 (4 KiB) or 1 (8 KiB) CTAs fit per SM and a batch's units are
-// resident in fewer waves.  Measured on GB300: 3-4 stages with fewer CTAs per SM
-// were 3-10 % slower on every benchmark workload.
+// A CTA's loads are served at a bounded rate for each warp's stages in flight
+// (measured on GB300: one 2 KiB K+V page pair per warp about every 0.5 us with the
+// page math, 2 to 4 stages alike), so the warps per CTA set how fast one long
+// sequence streams.  Head size 64: 8 warps (3 CTAs per SM); 128 and 256: 4 warps,
+// whose larger pages already fill HBM with 3 CTAs per SM.
+constexpr int mma_warps(int kind, int D) { return (void)kind, D == 64 ? 8 : 4; }
+// Two stages per warp: pages of 2-8 KiB give 35-131 KiB per CTA.  Measured on
+// GB300: 3-4 stages with fewer CTAs per SM were slower on every benchmark workload.
 constexpr int mma_stages(int kind, int D) { return (void)kind, (void)D, 2; }
 constexpr size_t kMmaScratch = 2048;  // sequence-order ranking scratch (after the barriers)
 constexpr size_t mma_smem(int kind, int D) {
@@ -88,6 +93,10 @@ cudaError_t launch_decode_mma_16(const DecodeParams &p, int kind, const CUtensor
 cudaError_t launch_decode_mma_fp8(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                   cudaStream_t st);  // KIND_FP8_*
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st);
+// Resident CTAs per SM of a tensor-core instantiation (CUDA occupancy calculator:
+// shared memory, registers and threads); 0 when it cannot be queried.
+int occupancy_decode_mma_16(int kind, int D);
+int occupancy_decode_mma_fp8(int kind, int D);
 
 // Launch `kern` as a programmatic dependent of the previous work on `st`, in
 // thread-block clusters of `cluster_x` CTAs along x when cluster_x > 1.

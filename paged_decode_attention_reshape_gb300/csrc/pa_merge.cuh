@@ -24,10 +24,31 @@ namespace pa {
 // Up to this many partitions the merge keeps the per-partition weights in shared memory.
 constexpr int kMergeSmemParts = 256;
 
+// Workspace rows of the partial states.  Row r holds (m, l) at part_ml[r] and acc at
+// part_acc[r * D .. r * D + D).
+// Fixed-size partitions: one row per (sequence, query head, partition).
+struct FixedRows {
+  int64_t head0;  // s * Hq + first head of the group
+  int max_parts;
+  __device__ __forceinline__ int64_t operator()(int hh, int i) const { return (head0 + hh) * max_parts + i; }
+};
+// Balanced split: each CTA owns two row groups (its first and its last page range),
+// 8 heads each; the parts of one sequence belong to consecutive CTAs c0, c0+1, ...,
+// and the first of them stores the sequence in its second group when the sequence
+// is not where its range starts (j0 = 1).
+struct FlatRows {
+  int64_t c0;  // head row * CTAs per head row + first CTA of the sequence
+  int j0;
+  __device__ __forceinline__ int64_t operator()(int hh, int i) const {
+    return ((c0 + i) * 2 + (i == 0 ? j0 : 0)) * 8 + hh;
+  }
+};
+
 // smem_w: shared memory for 8 * kMergeSmemParts floats, free for reuse by now.
-template <typename OutT, int D>
+// rows(hh, i): workspace row of head h0 + hh in the unit's i-th part.
+template <typename OutT, int D, typename Rows>
 __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int unit, int h0, int ng, int nparts,
-                                              float vs, int threads, float *smem_w) {
+                                              float vs, int threads, float *smem_w, Rows rows) {
   __shared__ int s_last;
   float(*s_w)[kMergeSmemParts] = reinterpret_cast<float(*)[kMergeSmemParts]>(smem_w);  // weight per head, part
   __syncthreads();  // every partial store of this CTA precedes thread 0's release below
@@ -45,14 +66,13 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = threads >> 5;
   const bool in_smem = nparts <= kMergeSmemParts;
   for (int hh = warp; hh < ng; hh += nw) {
-    const int64_t row0 = (static_cast<int64_t>(s) * p.Hq + h0 + hh) * p.max_parts;
     float M = -INFINITY;
-    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_ml + row0 + i).x);
+    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(p.part_ml + rows(hh, i)).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float den = 0.f;
     for (int i = lane; i < nparts; i += 32) {
-      const float2 v = __ldcg(p.part_ml + row0 + i);
+      const float2 v = __ldcg(p.part_ml + rows(hh, i));
       const float w = v.x == -INFINITY ? 0.f : ex2(v.x - M);
       den += w * v.y;
       if (in_smem) s_w[hh][i] = w;
@@ -71,16 +91,15 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int 
   __syncthreads();
   for (int i = threadIdx.x; i < ng * D; i += threads) {
     const int hh = i / D, d = i - hh * D;
-    const int64_t row0 = (static_cast<int64_t>(s) * p.Hq + h0 + hh) * p.max_parts;
-    const float *acc = p.part_acc + row0 * D + d;
     float r = 0.f;
     if (in_smem) {
-      for (int q = 0; q < nparts; ++q) r += s_w[hh][q] * __ldcg(acc + static_cast<int64_t>(q) * D);
+      for (int q = 0; q < nparts; ++q) r += s_w[hh][q] * __ldcg(p.part_acc + rows(hh, q) * D + d);
     } else {
       const float M = s_w[hh][0];
       for (int q = 0; q < nparts; ++q) {
-        const float m = __ldcg(p.part_ml + row0 + q).x;
-        r += (m == -INFINITY ? 0.f : ex2(m - M)) * __ldcg(acc + static_cast<int64_t>(q) * D);
+        const int64_t r0 = rows(hh, q);
+        const float m = __ldcg(p.part_ml + r0).x;
+        r += (m == -INFINITY ? 0.f : ex2(m - M)) * __ldcg(p.part_acc + r0 * D + d);
       }
       r *= s_w[hh][1];
     }

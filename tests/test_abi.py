@@ -148,7 +148,10 @@ def test_partition_plan_rules(L):
     P, n = pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, 0)
     assert P >= 1024 and P % 16 == 0 and n == -(-8192 * 16 // P) and n > 8
     # heuristic: a batch that fits the resident slots gets its longest sequences cut in two
-    assert pa.pa_decode_plan(64, 32, 8, 64, 128, pa.PA_BF16, 152, 0) == (1024, 2)
+    assert pa.pa_decode_plan(64, 32, 8, 128, 128, pa.PA_BF16, 300, 0) == (1024, 2)
+    # heuristic: a longest-first batch whose units fill the slots once (64 x 8 units, 152 x 3
+    # resident 8-warp CTAs at head size 64) is not split
+    assert pa.pa_decode_plan(64, 32, 8, 64, 128, pa.PA_BF16, 152, 0) == (0, 1)
     # heuristic: a partition as long as the table is no split
     assert pa.pa_decode_plan(64, 32, 8, 64, 64, pa.PA_BF16, 152, 0) == (0, 1)
     # heuristic: a longest-first batch whose units fill the resident slots is not split
@@ -158,6 +161,23 @@ def test_partition_plan_rules(L):
     # invalid arguments
     with pytest.raises(pa.PAError):
         pa.pa_decode_plan(4, 30, 8, 128, 64, pa.PA_BF16, 152, 0)
+
+
+def test_balanced_split_plan(L):
+    """PA_PARTITION_BALANCED: one resident wave of CTAs per (kv head, head group) row.
+    Without a device the resident CTAs per SM are the shared-memory bound:
+    D=64 bf16 pages 2 KiB -> 8 warps x 2 stages x 4 KiB + 3 KiB = 67 KiB -> 3 per SM;
+    D=128 bf16 -> 4 warps x 2 stages x 8 KiB + 3 KiB = 67 KiB -> 3 per SM."""
+    B = pa.PA_PARTITION_BALANCED
+    assert pa.pa_decode_plan(64, 32, 8, 64, 128, pa.PA_BF16, 152, B) == (B, 152 * 3 // 8)
+    assert pa.pa_decode_plan(4, 32, 8, 128, 8192, pa.PA_BF16, 152, B) == (B, 152 * 3 // 8)
+    assert pa.pa_decode_plan(4, 32, 2, 128, 8192, pa.PA_BF16, 152, B) == (B, 152 * 3 // 4)   # 2 groups per KV head
+    assert pa.pa_decode_plan(1, 1024, 1024, 128, 8, pa.PA_BF16, 10, B) == (B, 1)              # fewer slots than rows
+    assert pa.pa_decode_plan(511, 32, 8, 64, 128, pa.PA_BF16, 152, B)[0] == B
+    with pytest.raises(pa.PAError) as e:                                                      # batch limit
+        pa.pa_decode_plan(512, 32, 8, 64, 128, pa.PA_BF16, 152, B)
+    assert e.value.status == -7
+    assert pa.pa_decode_plan(4, 32, 8, 128, 64, pa.PA_F32, 152, B) == (0, 1)                 # fp32 kernel: unsplit
 
 
 def test_workspace_size(L):

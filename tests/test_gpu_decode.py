@@ -13,8 +13,8 @@ import paged_decode_attention_reshape_gb300 as pa
 pytestmark = pytest.mark.gpu
 
 LENS = [0, 1, 15, 16, 17, 33, 100, 257, 700, 1100]   # empty, single token, ragged tails, several tiles
-PARTS = [-1, 16, 64, 512, 0, -2, -4, -8]              # unsplit, splits of 1/4/32 pages, heuristic,
-                                                      # cluster splits into 2/4/8 equal parts
+PARTS = [-1, 16, 64, 512, 0, -2, -4, -8, -100]       # unsplit, splits of 1/4/32 pages, heuristic,
+                                                      # cluster splits into 2/4/8 equal parts, balanced
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -137,3 +137,69 @@ def test_seq_len_beyond_table_is_reported():
     run(c, g, -1)
     rc, bits = pa.pa_check_device_error(g.err)
     assert rc == -6 and bits & pa.PA_DEVERR_SEQLEN_RANGE
+
+
+def _checked(c, g, P, out=None):
+    o = run(c, g, P, out=out)
+    torch.cuda.synchronize()
+    rc, bits = pa.pa_check_device_error(g.err)
+    assert rc == 0, (P, rc, bits)
+    return o.double().cpu().numpy()
+
+
+BAL = pa.PA_PARTITION_BALANCED
+
+
+@pytest.mark.parametrize("lens", [
+    [0, 0, 0],                                   # nothing to read: all-zero rows
+    [1, 0, 17],                                  # 3 pages in all, fewer than the CTAs of a row
+    [5000] + [1] * 40 + [0, 0, 0] + [300],       # one long sequence over many CTAs, many 1-page ones
+    [16] * 57 + [2000, 15, 0, 33],               # boundaries on page edges, several sequences per CTA
+], ids=["all_empty", "fewer_pages_than_ctas", "long_and_short", "many_per_cta"])
+def test_balanced_split_edges(lens):
+    c = make_case(len(lens), 32, 8, 128, lens, seed=len(lens) * 7 + 1)
+    ref = reference(c)
+    g = to_gpu(c)
+    g.out.fill_(float("nan"))
+    got = _checked(c, g, BAL)
+    assert_close(got, ref, "balanced")
+    assert_close(got, _checked(c, g, -1), "balanced vs unsplit")
+
+
+def test_balanced_split_largest_batch_and_limit():
+    rng = np.random.default_rng(511)
+    lens = rng.integers(0, 200, size=511).tolist()
+    c = make_case(511, 8, 2, 64, lens, seed=511)
+    g = to_gpu(c)
+    assert_close(_checked(c, g, BAL), reference(c), "511 sequences")
+    c2 = make_case(512, 8, 2, 64, [1] * 512, seed=512)
+    g2 = to_gpu(c2)
+    with pytest.raises(pa.PAError) as e:
+        run(c2, g2, BAL)
+    assert e.value.status == -7
+
+
+def test_balanced_split_repeats_and_recovers_after_errors():
+    """The arrival counters return to zero after every call, after calls with a bad block id
+    or a bad length too: the same workspace then gives the right result again."""
+    lens = [700, 33, 1500, 2, 260]
+    for fp8 in (False, True):
+        c = make_case(5, 64 if fp8 else 32, 8, 128, lens, fp8=fp8, seed=77, k_scale=0.05, v_scale=0.05)
+        ref = reference(c)
+        g = to_gpu(c)
+        outs = [_checked(c, g, BAL) for _ in range(3)]
+        for o in outs:
+            assert_close(o, ref, "repeat fp8=%s" % fp8)
+        assert all(np.array_equal(outs[0], o) for o in outs[1:])
+        good_bt, good_sl = g.block_table.clone(), g.seq_lens.clone()
+        g.block_table[2, 40] = c.NB + 3
+        run(c, g, BAL)
+        rc, bits = pa.pa_check_device_error(g.err)
+        assert rc == -6 and bits & pa.PA_DEVERR_BLOCK_RANGE
+        g.block_table.copy_(good_bt)
+        g.seq_lens[1] = c.maxNB * 16 + 1
+        run(c, g, BAL)
+        rc, bits = pa.pa_check_device_error(g.err)
+        assert rc == -6 and bits & pa.PA_DEVERR_SEQLEN_RANGE
+        g.seq_lens.copy_(good_sl)
+        assert_close(_checked(c, g, BAL), ref, "after errors fp8=%s" % fp8)
