@@ -56,6 +56,7 @@
 namespace pa {
 
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before a wait gives up (>= ~20 ms)
+constexpr float kMaxSlack = 8.f;            // log2 units: probabilities within a page stay <= 256
 
 template <int KIND, int D, int W, int STAGES>
 struct MmaCfg {
@@ -261,20 +262,22 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
     const float s1 = va ? (c0[1] + c1[1]) * sc1 : -INFINITY;
     const float s2 = vb8 ? (c0[2] + c1[2]) * sc0 : -INFINITY;
     const float s3 = vb8 ? (c0[3] + c1[3]) * sc1 : -INFINITY;
-    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+    // The running max of a head moves only when a score exceeds it by more than
+    // kMaxSlack (log2 units); otherwise the page is weighted against the stale max,
+    // p = 2^(s - m) <= 2^kMaxSlack, and the cross-lane max reduction and the rescale
+    // are skipped.  (m, l, acc) stay consistent, so the merges are unchanged.
+    const float lm0 = fmaxf(s0, s2), lm1 = fmaxf(s1, s3);
+    if (__any_sync(0xffffffffu, (lm0 > m0 + kMaxSlack) | (lm1 > m1 + kMaxSlack))) {
+      float mx0 = lm0, mx1 = lm1;
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // 0 on the first page (m = -inf)
-    const float p0 = ex2(s0 - mn0), p1 = ex2(s1 - mn1), p2 = ex2(s2 - mn0), p3 = ex2(s3 - mn1);
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
-    m0 = mn0;
-    m1 = mn1;
-    if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {  // some running max moved
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // 0 on the first page (m = -inf)
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int t = 0; t < C::KT; ++t) {
         acc[t][0] *= al0;
@@ -282,7 +285,12 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
         acc[t][2] *= al0;
         acc[t][3] *= al1;
       }
+      m0 = mn0;
+      m1 = mn1;
     }
+    const float p0 = ex2(s0 - m0), p1 = ex2(s1 - m1), p2 = ex2(s2 - m0), p3 = ex2(s3 - m1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
 
     // ---- P^T operand: hi + lo 16-bit halves, transposed in registers
     uint32_t bh0, bh1, bl0, bl1;
@@ -441,7 +449,7 @@ __device__ __forceinline__ void zero_rows(const DecodeParams &p, int s, int h0, 
 }
 
 template <int KIND, int D, int W, int STAGES>
-__global__ void __launch_bounds__(W * 32)
+__global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
   using C = MmaCfg<KIND, D, W, STAGES>;

@@ -81,6 +81,13 @@ constexpr int mma_warps(int kind, int D) { return (void)kind, D == 64 ? 8 : 4; }
 // Two stages per warp: pages of 2-8 KiB give 35-131 KiB per CTA.  Measured on
 // GB300: 3-4 stages with fewer CTAs per SM were slower on every benchmark workload.
 constexpr int mma_stages(int kind, int D) { return (void)kind, (void)D, 2; }
+// Resident CTAs per SM the register allocation must allow (ptxas launch bound): as
+// many as the shared memory admits, so registers never cut the occupancy, except
+// for the E4M3 head-size-128 kernel (6 by shared memory; held at 4 to avoid spills).
+constexpr bool mma_fp8(int kind) { return kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q; }
+constexpr int mma_min_ctas(int kind, int D) {
+  return D == 64 ? 3 : D == 128 ? (mma_fp8(kind) ? 4 : 3) : (mma_fp8(kind) ? 3 : 1);
+}
 constexpr size_t kMmaScratch = 2048;  // sequence-order ranking scratch (after the barriers)
 constexpr size_t mma_smem(int kind, int D) {
   return 1024 + static_cast<size_t>(mma_warps(kind, D)) * mma_stages(kind, D) *
