@@ -58,6 +58,10 @@ def lib() -> ctypes.CDLL:
             L.orc_partial_decode.argtypes = [P, P, P, i64, i64, i32, i32, i32, dbl, P, P, P]
             L.orc_lse_merge.restype = None
             L.orc_lse_merge.argtypes = [P, P, P, i32, i32, P]
+            L.orc_write_flat_heads.restype = i32
+            L.orc_write_flat_heads.argtypes = [P, i32, i64, i64, i32, i32, P, i64, P, i32, P]
+            L.orc_attention_causal.restype = i32
+            L.orc_attention_causal.argtypes = [P, P, P, i64, i64, i32, i32, i32, dbl, P, P]
             L.orc_paged_walk_decode.restype = i32
             L.orc_paged_walk_decode.argtypes = [P, P, P, P, i32, i64, i32, i32, i32, dbl, P]
             _lib = L
@@ -96,10 +100,11 @@ def quantize_e4m3(x, scale: float) -> np.ndarray:
 # --------------------------------------------------------------------- write
 
 def write_flat(rows: np.ndarray, rows_dtype: str, slots: np.ndarray, cache_flat: np.ndarray,
-               cache_dtype: str, scale: float = 1.0) -> None:
+               cache_dtype: str, scale=1.0) -> None:
     """rows [T, Hkv, D] (or a view with a token stride); cache_flat [num_slots, Hkv, D].
 
-    Writes in place.  Raises on a slot >= num_slots.
+    scale: one fp32 scale, or a sequence of Hkv per-head scales (head h quantises with
+    scale[h]).  Writes in place.  Raises on a slot >= num_slots.
     """
     assert rows.ndim == 3 and cache_flat.ndim == 3
     assert rows.strides[2] == rows.itemsize and rows.strides[1] == rows.shape[2] * rows.itemsize
@@ -109,9 +114,14 @@ def write_flat(rows: np.ndarray, rows_dtype: str, slots: np.ndarray, cache_flat:
     row_stride = rows.strides[0] // rows.itemsize
     sl = np.ascontiguousarray(slots, dtype=np.int64)
     assert sl.shape == (T,)
-    rc = lib().orc_write_flat(rows.ctypes.data_as(ctypes.c_void_p), _DT[rows_dtype], T, row_stride, Hkv, D,
-                              _ptr(sl), cache_flat.shape[0], _ptr(cache_flat), _DT[cache_dtype],
-                              float(np.float32(scale)))
+    args = (rows.ctypes.data_as(ctypes.c_void_p), _DT[rows_dtype], T, row_stride, Hkv, D,
+            _ptr(sl), cache_flat.shape[0], _ptr(cache_flat), _DT[cache_dtype])
+    if np.ndim(scale) == 0:
+        rc = lib().orc_write_flat(*args, float(np.float32(scale)))
+    else:
+        sc = np.ascontiguousarray(scale, dtype=np.float32)
+        assert sc.shape == (Hkv,)
+        rc = lib().orc_write_flat_heads(*args, _ptr(sc))
     if rc != 0:
         raise ValueError("orc_write_flat failed with %d" % rc)
 
@@ -131,6 +141,23 @@ def dense_decode(q, K, V, scale: float, return_probs: bool = False):
     if rc != 0:
         raise ValueError("orc_dense_decode failed with %d" % rc)
     return (out, probs) if return_probs else out
+
+
+def attention_causal(q, K, V, scale: float, alibi_slopes=None) -> np.ndarray:
+    """n query tokens of one sequence: q [n, Hq, D], K/V [L, Hkv, D] -> out [n, Hq, D] (fp64).
+    Query i sits at position L - n + i and sees tokens 0 .. L - n + i; alibi_slopes [Hq]
+    adds slope_h * (t - (L - n + i)) to the logits."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    n, Hq, D = q.shape
+    L, Hkv, D2 = K.shape
+    assert D2 == D and V.shape == K.shape
+    sl = None if alibi_slopes is None else _f64(alibi_slopes)
+    out = np.zeros((n, Hq, D), dtype=np.float64)
+    rc = lib().orc_attention_causal(_ptr(q), _ptr(K), _ptr(V), n, L, Hq, Hkv, D, float(scale),
+                                    _ptr(sl) if sl is not None else None, _ptr(out))
+    if rc != 0:
+        raise ValueError("orc_attention_causal failed with %d" % rc)
+    return out
 
 
 def partial_decode(q, K, V, t0: int, t1: int, scale: float):
@@ -173,8 +200,9 @@ def paged_walk_decode(q, pool_k, pool_v, block_table_row, block_size: int, L: in
 
 # ------------------------------------------------------- cache element values
 
-def cache_values(cache_flat: np.ndarray, cache_dtype: str, scale: float = 1.0) -> np.ndarray:
-    """Element values of a flat cache in fp64 (E4M3 codes are decoded and multiplied by scale)."""
+def cache_values(cache_flat: np.ndarray, cache_dtype: str, scale=1.0) -> np.ndarray:
+    """Element values of a flat cache [n, Hkv, D] in fp64 (E4M3 codes are decoded and multiplied
+    by the scale: one fp32 value, or Hkv per-head values)."""
     if cache_dtype == "f32":
         return cache_flat.astype(np.float64)
     if cache_dtype == "bf16":
@@ -183,5 +211,8 @@ def cache_values(cache_flat: np.ndarray, cache_dtype: str, scale: float = 1.0) -
         return cache_flat.view(np.float16).astype(np.float64)
     if cache_dtype == "e4m3":
         table = e4m3_decode(np.arange(256, dtype=np.uint8))
-        return table[cache_flat] * float(np.float32(scale))
+        if np.ndim(scale) == 0:
+            return table[cache_flat] * float(np.float32(scale))
+        sc = np.asarray(scale, dtype=np.float32).astype(np.float64)
+        return table[cache_flat] * sc.reshape((1, -1) + (1,) * (cache_flat.ndim - 2))
     raise ValueError(cache_dtype)

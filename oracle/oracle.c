@@ -39,6 +39,21 @@
  *    kernel: paged KV cache & block tables", Code).  Used only to check the
  *    oracle itself: paged == dense for any physical permutation.
  *
+ *  - orc_write_flat_heads: the write with one FP8 scale per KV head ("Inside
+ *    vLLM CUDA Kernels", Part 2, why layout and quantization scale produce two
+ *    copy paths: kv_scale_stride == 0 means every head shares one scale,
+ *    otherwise head h uses scale[h * kv_scale_stride]).
+ *
+ *  - orc_attention_causal: n query tokens of one sequence over its L K/V rows.
+ *    Query i sits at position L - n + i and sees tokens t <= L - n + i (the
+ *    varlen read path of "Inside vLLM CUDA Kernels", Part 3: query_start_loc
+ *    packs a request's new tokens, seq_lens bounds the visible history; the
+ *    reading taken here is the usual causal mask with the new tokens at the end
+ *    of the history).  With ALiBi ("vLLM 源码完全拆解（七）", the QK step: the
+ *    kernel adds the head's slope a_h times the token's non-positive distance
+ *    from the current position, which has bias 0), the logit is
+ *    scale * q_i . k_t + a_h * (t - (L - n + i)).  n = 1 is single-query decode.
+ *
  *  - orc_partial_decode / orc_lse_merge: the split-KV form -- the unnormalised
  *    state (m, l, acc) of one token range, and the max/log-sum-exp merge of
  *    several ranges ("Inside vLLM CUDA Kernels", Part 3, "Split-KV changes the
@@ -338,6 +353,92 @@ int orc_paged_walk_decode(const double *q, const double *pool_k, const double *p
         if (L > 0)
             for (int d = 0; d < D; ++d)
                 o[d] /= l;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------- per-head scales, causal */
+
+/*
+ * orc_write_flat with one scale per KV head: head h of every row quantises with
+ * scales[h].  Same arguments otherwise; scales is [Hkv].
+ */
+int orc_write_flat_heads(const void *rows, int rows_dtype, int64_t T, int64_t row_stride,
+                         int Hkv, int D, const int64_t *slots, int64_t num_slots,
+                         void *cache_flat, int cache_dtype, const float *scales)
+{
+    int rb = elem_bytes(rows_dtype), cb = elem_bytes(cache_dtype);
+    if (cache_dtype != rows_dtype && cache_dtype != ORC_E4M3)
+        return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots)
+            return -1;
+        for (int h = 0; h < Hkv; ++h) {
+            for (int d = 0; d < D; ++d) {
+                int64_t src = t * row_stride + (int64_t)h * D + d;
+                int64_t dst = (slot * Hkv + h) * (int64_t)D + d;
+                if (cache_dtype == rows_dtype)
+                    memcpy((char *)cache_flat + dst * cb, (const char *)rows + src * rb, (size_t)rb);
+                else
+                    ((uint8_t *)cache_flat)[dst] = orc_quantize_e4m3(load_elem(rows, rows_dtype, src), scales[h]);
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * n query tokens of one sequence, causal, optional ALiBi.  q: [n, Hq, D];
+ * K, V: [L, Hkv, D] in logical order; slopes: [Hq] or NULL; out: [n, Hq, D].
+ * Query i (position L - n + i) sees tokens 0 .. L - n + i:
+ *   z_t = scale * q_i . k_t + slope_h * (t - (L - n + i)),  o = sum_t softmax(z)_t v_t.
+ * Returns -1 if Hq is not a multiple of Hkv, -2 if n > L.
+ */
+int orc_attention_causal(const double *q, const double *K, const double *V, int64_t n, int64_t L,
+                         int Hq, int Hkv, int D, double scale, const double *slopes, double *out)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0)
+        return -1;
+    if (n > L)
+        return -2;
+    int G = Hq / Hkv;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t pos = L - n + i;             /* this query's position; it sees 0 .. pos */
+        for (int h = 0; h < Hq; ++h) {
+            int g = h / G;
+            const double *qh = q + (i * Hq + h) * (int64_t)D;
+            double *o = out + (i * Hq + h) * (int64_t)D;
+            double a = slopes ? slopes[h] : 0.0;
+            for (int d = 0; d < D; ++d)
+                o[d] = 0.0;
+            double M = -INFINITY;
+            for (int64_t t = 0; t <= pos; ++t) {
+                double z = 0.0;
+                for (int d = 0; d < D; ++d)
+                    z += qh[d] * K[(t * Hkv + g) * (int64_t)D + d];
+                z = z * scale + a * (double)(t - pos);
+                if (z > M)
+                    M = z;
+            }
+            double S = 0.0;
+            for (int64_t t = 0; t <= pos; ++t) {
+                double z = 0.0;
+                for (int d = 0; d < D; ++d)
+                    z += qh[d] * K[(t * Hkv + g) * (int64_t)D + d];
+                S += exp(z * scale + a * (double)(t - pos) - M);
+            }
+            for (int64_t t = 0; t <= pos; ++t) {
+                double z = 0.0;
+                for (int d = 0; d < D; ++d)
+                    z += qh[d] * K[(t * Hkv + g) * (int64_t)D + d];
+                double p = exp(z * scale + a * (double)(t - pos) - M) / S;
+                for (int d = 0; d < D; ++d)
+                    o[d] += p * V[(t * Hkv + g) * (int64_t)D + d];
+            }
+        }
     }
     return 0;
 }

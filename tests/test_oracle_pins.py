@@ -367,3 +367,101 @@ def test_quantize_near_rounding_midpoints(scale):
     ok = np.abs(y) < 464.0
     ref = torch.from_numpy(y[ok].copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(oracle.quantize_e4m3(x[ok], scale), ref)
+
+
+# ------------------------------------------ per-head scales, ALiBi, multi-query
+
+def test_write_per_head_scales():
+    """Head h quantises with its own scale ("Inside vLLM CUDA Kernels", Part 2: head h uses
+    scale[h * kv_scale_stride]): each head against the library's fp32 division and E4M3
+    conversion with that head's scale; equal per-head scales give the per-tensor write."""
+    T, Hkv, D = 5, 4, 16
+    x = (RNG.standard_normal((T, Hkv, D)) * 3).astype(np.float32)
+    bf = (x.view(np.uint32) >> 16).astype(np.uint16)
+    vals = (bf.astype(np.uint32) << 16).view(np.float32)
+    scales = np.array([0.05, 0.37, 1.0, 3.0], dtype=np.float32)
+    slots = np.array([3, -1, 0, 7, 5])
+    cache = np.zeros((8, Hkv, D), dtype=np.uint8)
+    oracle.write_flat(bf, "bf16", slots, cache, "e4m3", scales)
+    for t, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        for h in range(Hkv):
+            y = (torch.from_numpy(vals[t, h].copy()) / torch.tensor(scales[h])).numpy()
+            assert np.abs(y).max() < 464.0
+            ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(cache[sl, h], ref), (t, h)
+    assert not cache[[1, 2, 4, 6]].any()
+    same, per_tensor = np.zeros_like(cache), np.zeros_like(cache)
+    oracle.write_flat(bf, "bf16", slots, same, "e4m3", np.full(Hkv, 0.37, np.float32))
+    oracle.write_flat(bf, "bf16", slots, per_tensor, "e4m3", 0.37)
+    assert np.array_equal(same, per_tensor)
+    # element values with per-head scales: the library's E4M3 decode times the head's scale
+    v = oracle.cache_values(cache, "e4m3", scales)
+    lib_vals = torch.from_numpy(cache.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    assert np.array_equal(v, lib_vals * scales.astype(np.float64)[None, :, None])
+
+
+def test_alibi_closed_form():
+    """q = 0 makes every dot product 0, so the weights are exp(a (t - (L - 1))) normalised: a
+    geometric distribution with ratio e^-a, ending at the current position (bias 0).  With
+    V[t] = e_t the output is that distribution."""
+    L, D = 12, 16
+    for a in (0.0, 0.25, 1.5, 40.0):
+        q = np.zeros((1, 1, D))
+        K = RNG.standard_normal((L, 1, D))
+        V = np.zeros((L, 1, D))
+        V[np.arange(L), 0, np.arange(L)] = 1.0
+        out = oracle.attention_causal(q, K, V, 0.7, alibi_slopes=[a])[0, 0]
+        r = math.exp(-a)
+        ref = np.array([r ** (L - 1 - t) for t in range(L)])
+        ref /= ref.sum()
+        assert np.allclose(out[:L], ref, rtol=1e-12, atol=1e-300) and not out[L:].any()
+
+
+def test_alibi_decode_vs_scipy_softmax_and_zero_slopes():
+    L, Hq, Hkv, D = 40, 4, 2, 16
+    q, K, V = _rand(L, Hq, Hkv, D)
+    slopes = np.array([0.5, 0.0625, 2.0 ** -8, 1.0])
+    out = oracle.attention_causal(q[None], K, V, 0.25, slopes)[0]
+    G = Hq // Hkv
+    for h in range(Hq):
+        z = 0.25 * (K[:, h // G, :] @ q[h]) + slopes[h] * (np.arange(L) - (L - 1))
+        assert np.allclose(out[h], softmax(z) @ V[:, h // G, :], rtol=1e-12, atol=1e-13)
+    # zero slopes (or none): single-query decode
+    assert np.array_equal(oracle.attention_causal(q[None], K, V, 0.25, np.zeros(Hq))[0],
+                          oracle.attention_causal(q[None], K, V, 0.25)[0])
+    assert np.allclose(oracle.attention_causal(q[None], K, V, 0.25)[0], oracle.dense_decode(q, K, V, 0.25),
+                       rtol=1e-13, atol=1e-14)
+
+
+def test_causal_whole_prompt_vs_masked_matrix():
+    """n = L (a whole prompt): the textbook masked form softmax(scale Q K^T + bias + M) V, M the
+    strictly-upper-triangular -inf mask, bias a_h (j - i)."""
+    L, Hq, Hkv, D = 9, 4, 2, 8
+    q = RNG.standard_normal((L, Hq, D))
+    K = RNG.standard_normal((L, Hkv, D))
+    V = RNG.standard_normal((L, Hkv, D))
+    slopes = np.array([0.0, 0.5, 0.125, 2.0])
+    out = oracle.attention_causal(q, K, V, 0.3, slopes)
+    G = Hq // Hkv
+    idx = np.arange(L)
+    for h in range(Hq):
+        Z = 0.3 * q[:, h, :] @ K[:, h // G, :].T + slopes[h] * (idx[None, :] - idx[:, None])
+        Z[np.triu_indices(L, 1)] = -np.inf
+        assert np.allclose(out[:, h, :], softmax(Z, axis=1) @ V[:, h // G, :], rtol=1e-12, atol=1e-13)
+
+
+def test_causal_chunk_rows_are_prefix_decodes():
+    """n < L (new tokens at the end of a history): query i is single-query decode over the
+    first L - n + i + 1 tokens; more queries than history is refused."""
+    L, n, Hq, Hkv, D = 30, 5, 8, 2, 16
+    q = RNG.standard_normal((n, Hq, D))
+    K = RNG.standard_normal((L, Hkv, D))
+    V = RNG.standard_normal((L, Hkv, D))
+    out = oracle.attention_causal(q, K, V, 0.2)
+    for i in range(n):
+        vis = L - n + i + 1
+        assert np.allclose(out[i], oracle.dense_decode(q[i], K[:vis], V[:vis], 0.2), rtol=1e-13, atol=1e-14)
+    with pytest.raises(ValueError):
+        oracle.attention_causal(np.zeros((4, 2, 8)), np.zeros((3, 1, 8)), np.zeros((3, 1, 8)), 1.0)
