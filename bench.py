@@ -82,16 +82,22 @@ def stage(w, device="cuda", history=True, poison=True) -> Staged:
     st = Staged()
     st.w = w
     cdt = _torch_dt(w.cache_dtype)
-    shape = (w.num_blocks, w.Hkv, configs.BLOCK, w.D)
-    st.k_cache = torch.empty(shape, dtype=cdt, device=device)
-    st.v_cache = torch.empty(shape, dtype=cdt, device=device)
+    nhd = w.layout == "nhd"
+    shape = (w.num_blocks, configs.BLOCK, w.Hkv, w.D) if nhd else (w.num_blocks, w.Hkv, configs.BLOCK, w.D)
+    kb = torch.empty(shape, dtype=cdt, device=device)
+    vb = torch.empty(shape, dtype=cdt, device=device)
     if poison:
-        nan_fill_(st.k_cache)
-        nan_fill_(st.v_cache)
+        nan_fill_(kb)
+        nan_fill_(vb)
+    # the library takes every cache as [NB, Hkv, 16, D]; an NHD cache is passed as that permutation
+    st.k_cache = kb.permute(0, 2, 1, 3) if nhd else kb
+    st.v_cache = vb.permute(0, 2, 1, 3) if nhd else vb
     st.fp8 = w.kv_dtype == "e4m3"
     st.kv_mode = pa.PA_KV_FP8_E4M3 if st.fp8 else pa.PA_KV_AUTO
-    st.k_scale = torch.tensor([w.k_scale], dtype=torch.float32, device=device)
-    st.v_scale = torch.tensor([w.v_scale], dtype=torch.float32, device=device)
+    st.k_scale = torch.tensor(np.atleast_1d(w.k_scales()), dtype=torch.float32, device=device)
+    st.v_scale = torch.tensor(np.atleast_1d(w.v_scales()), dtype=torch.float32, device=device)
+    st.scale_stride = 0 if w.k_head_scales is None else 1
+    st.alibi = None if w.alibi is None else torch.from_numpy(w.alibi).to(device)
     st.err = torch.zeros(1, dtype=torch.int32, device=device)
     bt = w.block_table.copy()
     st.block_table = torch.from_numpy(bt).to(device)
@@ -116,9 +122,19 @@ def write_history(st: Staged, device="cuda", rows_per_call=1 << 16) -> None:
             pos = torch.arange(p0, p1, dtype=torch.int64)
             K, V = data.history_rows(w, s, device, positions=pos)
             slots = torch.from_numpy(w.slot_of(s, np.arange(p0, p1))).to(device)
-            pa.pa_reshape_and_cache(K, V, st.k_cache, st.v_cache, slots, st.kv_mode, st.k_scale, st.v_scale,
-                                    st.err)
+            write_rows(st, K, V, slots)
     torch.cuda.synchronize()
+
+
+def write_rows(st: Staged, K, V, slots) -> None:
+    """Cache write of rows K/V [n, Hkv, D] at `slots` (the plain entry point unless the
+    workload has per-head scales)."""
+    import paged_decode_attention_reshape_gb300 as pa
+    if st.scale_stride:
+        pa.pa_reshape_and_cache_opt(K, V, st.k_cache, st.v_cache, slots, st.kv_mode, st.k_scale, st.v_scale,
+                                    st.scale_stride, st.err)
+    else:
+        pa.pa_reshape_and_cache(K, V, st.k_cache, st.v_cache, slots, st.kv_mode, st.k_scale, st.v_scale, st.err)
 
 
 def workspace_for(st: Staged, partition_size: int):
@@ -133,17 +149,20 @@ def workspace_for(st: Staged, partition_size: int):
 
 
 def run_write(st: Staged) -> None:
-    import paged_decode_attention_reshape_gb300 as pa
-    pa.pa_reshape_and_cache(st.k_step, st.v_step, st.k_cache, st.v_cache, st.slot_mapping, st.kv_mode,
-                            st.k_scale, st.v_scale, st.err)
+    write_rows(st, st.k_step, st.v_step, st.slot_mapping)
 
 
 def run_decode(st: Staged, partition_size: int = 0, ws=None, out=None) -> None:
     import paged_decode_attention_reshape_gb300 as pa
     w = st.w
-    pa.pa_decode_ex(st.out if out is None else out, st.q, st.k_cache, st.v_cache, st.block_table, st.seq_lens,
-                    w.scale, w.Hkv, st.k_scale if st.fp8 else None, st.v_scale if st.fp8 else None,
-                    partition_size, ws, st.err)
+    o = st.out if out is None else out
+    ks, vs = (st.k_scale, st.v_scale) if st.fp8 else (None, None)
+    if st.scale_stride or st.alibi is not None:
+        pa.pa_decode_opt(o, st.q, st.k_cache, st.v_cache, st.block_table, st.seq_lens, w.scale, w.Hkv, ks, vs,
+                         st.scale_stride, st.alibi, partition_size, ws, st.err)
+    else:
+        pa.pa_decode_ex(o, st.q, st.k_cache, st.v_cache, st.block_table, st.seq_lens, w.scale, w.Hkv, ks, vs,
+                        partition_size, ws, st.err)
 
 
 def run_step(st: Staged, partition_size: int = 0, ws=None) -> None:
@@ -335,11 +354,14 @@ def cpu_baseline(w, target_s=12.0, max_seqs=None):
         if kind == "e4m3":
             ck = np.zeros((L, w.Hkv, w.D), dtype=np.uint8)
             cv = np.zeros((L, w.Hkv, w.D), dtype=np.uint8)
-            oracle.write_flat(K, "bf16", np.arange(L), ck, "e4m3", w.k_scale)
-            oracle.write_flat(V, "bf16", np.arange(L), cv, "e4m3", w.v_scale)
-            K = oracle.cache_values(ck, "e4m3", w.k_scale)
-            V = oracle.cache_values(cv, "e4m3", w.v_scale)
-        oracle.dense_decode(qs[s], K, V, w.scale)
+            oracle.write_flat(K, "bf16", np.arange(L), ck, "e4m3", w.k_scales())
+            oracle.write_flat(V, "bf16", np.arange(L), cv, "e4m3", w.v_scales())
+            K = oracle.cache_values(ck, "e4m3", w.k_scales())
+            V = oracle.cache_values(cv, "e4m3", w.v_scales())
+        if w.alibi is not None:
+            oracle.attention_causal(qs[s][None], K, V, w.scale, w.alibi)
+        else:
+            oracle.dense_decode(qs[s], K, V, w.scale)
         return L
 
     # calibrate on one sequence, then size the sample to about target_s of wall time; a

@@ -123,6 +123,35 @@ int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa_tensor
                          pa_stream_t stream);
 
 /*
+ * Options of the _opt entry points.  Zero-initialise the struct (every field then
+ * takes its default) and set what the call needs.
+ *
+ * Per-head scales ("Inside vLLM CUDA Kernels", Part 2, why layout and quantization
+ * scale produce two copy paths: kv_scale_stride == 0 means every head shares one
+ * scale, otherwise head h uses scale[h * kv_scale_stride]).
+ */
+typedef struct {
+    const float *k_scale;  /* device fp32 scale(s) of an FP8 cache; NULL = 1.0 */
+    const float *v_scale;
+    int64_t scale_stride;  /* 0: one scale for every KV head; > 0: KV head h uses
+                              k_scale[h * scale_stride] and v_scale[h * scale_stride];
+                              < 0: PA_ERR_INVALID_ARG */
+    int *device_error;     /* device int to OR error bits into, or NULL */
+} pa_write_options;
+
+/*
+ * pa_reshape_and_cache_opt -- pa_reshape_and_cache with per-head FP8 scales.
+ * Arguments as pa_reshape_and_cache; `opt` may be NULL (all defaults).  An FP8
+ * element x of KV head h is stored as E4M3(fp32(x) / scale_h), scale_h as above.
+ * The cache may also be a strided view: an NHD cache [num_blocks, 16, Hkv, D]
+ * is passed as its [num_blocks, Hkv, 16, D] permutation (strides 16*Hkv*D, D,
+ * Hkv*D, 1).
+ */
+int pa_reshape_and_cache_opt(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache,
+                             pa_tensor *v_cache, const pa_tensor *slot_mapping, int kv_dtype,
+                             const pa_write_options *opt, pa_stream_t stream);
+
+/*
  * pa_decode -- single-query paged decode attention (one query token per sequence).
  *
  * Defined by: "Inside vLLM CUDA Kernels", Part 3 (scores = q k^T * scale,
@@ -191,6 +220,34 @@ int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, c
                  const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
                  const float *k_scale, const float *v_scale, int partition_size, void *workspace,
                  size_t workspace_bytes, int *device_error, pa_stream_t stream);
+
+/*
+ * Decode options (pa_decode_opt).  Zero-initialise, then set what is needed.
+ *
+ * ALiBi ("vLLM 源码完全拆解（七）", the QK step: the kernel adds a_h times the
+ * (non-positive) distance of key token t from the current position seq_len - 1 to
+ * the scaled logit, before the softmax): with alibi_slopes, the logit of query head
+ * h for key token t is scale * q.k_t + alibi_slopes[h] * (t - (seq_len - 1)).
+ */
+typedef struct {
+    const float *k_scale;        /* as pa_write_options: FP8 dequantisation scales, */
+    const float *v_scale;        /* NULL = 1.0; element value = code value * scale_h */
+    int64_t scale_stride;        /* 0: one scale; > 0: KV head h uses [h * scale_stride] */
+    const float *alibi_slopes;   /* device fp32 [Hq], contiguous, or NULL (no bias) */
+    int partition_size;          /* as pa_decode_ex (0 = the library's plan) */
+    void *workspace;             /* as pa_decode_ex; NULL with 0 bytes = the library's */
+    size_t workspace_bytes;      /*   internal workspace (pa_decode's) */
+    int *device_error;           /* device int to OR error bits into, or NULL */
+} pa_decode_options;
+
+/*
+ * pa_decode_opt -- pa_decode with every option.  Arguments as pa_decode; `opt`
+ * may be NULL (all defaults, as pa_decode).  Status codes as pa_decode_ex.  The
+ * cache may be an NHD cache passed as its [num_blocks, Hkv, 16, D] permutation.
+ */
+int pa_decode_opt(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                  const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                  const pa_decode_options *opt, pa_stream_t stream);
 
 /*
  * pa_decode_noalloc -- pa_decode_ex for callers that cannot allocate device memory.

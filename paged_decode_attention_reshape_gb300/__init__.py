@@ -29,9 +29,9 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED_DTYPE", 
           -4: "PA_ERR_WORKSPACE", -5: "PA_ERR_CUDA", -6: "PA_ERR_DEVICE_BOUNDS", -7: "PA_ERR_UNSUPPORTED_SHAPE",
           -8: "PA_ERR_DEVICE_TIMEOUT"}
 
-EXPORTS = ("pa_reshape_and_cache", "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_plan",
-           "pa_decode_workspace_size", "pa_check_device_error", "pa_status_string", "pa_profile_enable",
-           "pa_profile_read")
+EXPORTS = ("pa_reshape_and_cache", "pa_reshape_and_cache_opt", "pa_decode", "pa_decode_ex", "pa_decode_opt",
+           "pa_decode_noalloc", "pa_decode_plan", "pa_decode_workspace_size", "pa_check_device_error",
+           "pa_status_string", "pa_profile_enable", "pa_profile_read")
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 PA_PARTITION_BALANCED = -100  # partition_size: balanced split over one resident wave
 
@@ -44,6 +44,18 @@ if hasattr(torch, "float8_e4m3fn"):
 class PaTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 5), ("stride", ctypes.c_int64 * 5)]
+
+
+class PaWriteOptions(ctypes.Structure):
+    _fields_ = [("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("scale_stride", ctypes.c_int64),
+                ("device_error", ctypes.c_void_p)]
+
+
+class PaDecodeOptions(ctypes.Structure):
+    _fields_ = [("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("scale_stride", ctypes.c_int64),
+                ("alibi_slopes", ctypes.c_void_p), ("partition_size", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("device_error", ctypes.c_void_p)]
 
 
 class PAError(RuntimeError):
@@ -73,6 +85,10 @@ def lib() -> ctypes.CDLL:
             i32, f32 = ctypes.c_int, ctypes.c_float
             L.pa_reshape_and_cache.restype = i32
             L.pa_reshape_and_cache.argtypes = [T, T, T, T, T, i32, P, P, P, P]
+            L.pa_reshape_and_cache_opt.restype = i32
+            L.pa_reshape_and_cache_opt.argtypes = [T, T, T, T, T, i32, ctypes.POINTER(PaWriteOptions), P]
+            L.pa_decode_opt.restype = i32
+            L.pa_decode_opt.argtypes = [T, T, T, T, T, T, f32, i32, ctypes.POINTER(PaDecodeOptions), P]
             L.pa_decode.restype = i32
             L.pa_decode.argtypes = [T, T, T, T, T, T, f32, i32, P]
             L.pa_decode_ex.restype = i32
@@ -139,6 +155,34 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, kv_dtype: i
     rc = lib().pa_reshape_and_cache(*[ctypes.byref(a) for a in args], int(kv_dtype), _ptr(k_scale), _ptr(v_scale),
                                     _ptr(device_error), _stream(stream))
     _check(rc, "pa_reshape_and_cache")
+
+
+def pa_reshape_and_cache_opt(key, value, k_cache, v_cache, slot_mapping, kv_dtype: int = PA_KV_AUTO,
+                             k_scale=None, v_scale=None, scale_stride: int = 0, device_error=None,
+                             stream=None) -> None:
+    """pa_reshape_and_cache with per-head FP8 scales: KV head h uses k_scale[h * scale_stride]
+    (scale_stride 0: one scale for every head).  The cache may be a strided view (an NHD cache
+    [NB, 16, Hkv, D] passed as .permute(0, 2, 1, 3))."""
+    o = PaWriteOptions(_ptr(k_scale), _ptr(v_scale), int(scale_stride), _ptr(device_error))
+    args = (desc(key), desc(value), desc(k_cache), desc(v_cache), desc(slot_mapping))
+    rc = lib().pa_reshape_and_cache_opt(*[ctypes.byref(a) for a in args], int(kv_dtype), ctypes.byref(o),
+                                        _stream(stream))
+    _check(rc, "pa_reshape_and_cache_opt")
+
+
+def pa_decode_opt(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, num_kv_heads: int,
+                  k_scale=None, v_scale=None, scale_stride: int = 0, alibi_slopes=None, partition_size: int = 0,
+                  workspace=None, device_error=None, stream=None) -> None:
+    """pa_decode with every option: per-head FP8 scales (KV head h uses k_scale[h * scale_stride]),
+    ALiBi slopes (fp32 [Hq]: logit += slope_h * (t - (seq_len - 1))), partition size, caller
+    workspace (None: the library's internal one) and device error word."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    o = PaDecodeOptions(_ptr(k_scale), _ptr(v_scale), int(scale_stride), _ptr(alibi_slopes), int(partition_size),
+                        _ptr(workspace), ws_bytes, _ptr(device_error))
+    args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(block_table), desc(seq_lens))
+    rc = lib().pa_decode_opt(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), ctypes.byref(o),
+                             _stream(stream))
+    _check(rc, "pa_decode_opt")
 
 
 def pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, num_kv_heads: int,

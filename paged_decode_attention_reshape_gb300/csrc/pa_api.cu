@@ -117,15 +117,24 @@ EncodeTiledFn encode_fn() {
 
 // 4-D map over a [NB, Hkv, 16, D] cache: dims (D, 16, Hkv, NB), box (128 bytes, 16, 1, 1),
 // 128-byte swizzle.  One box = 16 token rows x 128 bytes = 2 KiB of one page.
-int make_cache_map(const pa_tensor *c, CUtensorMap *map) {
+// 4-D TMA map of one cache, boxes of one (block, kv head) page: 16 token rows of one
+// 128-byte swizzle span.  HND caches (token stride <= head stride) are described as
+// (D, 16, Hkv, NB), box (span, 16, 1, 1); NHD caches (token-major within a block,
+// [NB, 16, Hkv, D] seen through its [NB, Hkv, 16, D] permutation) in their own order,
+// (D, Hkv, 16, NB), box (span, 1, 16, 1), which lands in shared memory as the same
+// 16 x span tile.  *nhd tells the kernel which coordinate order to use.
+int make_cache_map(const pa_tensor *c, CUtensorMap *map, int *nhd) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PA_ERR_CUDA;
   const int eb = elem_bytes(c->dtype);
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(c->shape[3]), static_cast<cuuint64_t>(c->shape[2]),
-                              static_cast<cuuint64_t>(c->shape[1]), static_cast<cuuint64_t>(c->shape[0])};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(c->stride[2] * eb), static_cast<cuuint64_t>(c->stride[1] * eb),
+  *nhd = c->stride[2] > c->stride[1] ? 1 : 0;
+  const int mid_a = *nhd ? 1 : 2, mid_b = *nhd ? 2 : 1;  // dimension order after D
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(c->shape[3]), static_cast<cuuint64_t>(c->shape[mid_a]),
+                              static_cast<cuuint64_t>(c->shape[mid_b]), static_cast<cuuint64_t>(c->shape[0])};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(c->stride[mid_a] * eb),
+                                 static_cast<cuuint64_t>(c->stride[mid_b] * eb),
                                  static_cast<cuuint64_t>(c->stride[0] * eb)};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 16, 1, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), *nhd ? 1u : 16u, *nhd ? 16u : 1u, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUresult r = enc(map, dt, 4, c->data, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -318,9 +327,11 @@ PA_API const char *pa_status_string(int status) {
   }
 }
 
-PA_API int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache, pa_tensor *v_cache,
-                                const pa_tensor *slot_mapping, int kv_dtype, const float *k_scale,
-                                const float *v_scale, int *device_error, pa_stream_t stream) {
+PA_API int pa_reshape_and_cache_opt(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache,
+                                    pa_tensor *v_cache, const pa_tensor *slot_mapping, int kv_dtype,
+                                    const pa_write_options *opt, pa_stream_t stream) {
+  const pa_write_options o = opt ? *opt : pa_write_options{};
+  if (o.scale_stride < 0) return PA_ERR_INVALID_ARG;
   int r;
   if ((r = check_desc(key, 3)) || (r = check_desc(value, 3)) || (r = check_desc(slot_mapping, 1))) return r;
   int NB, Hkv, D;
@@ -369,9 +380,10 @@ PA_API int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa
   p.vc_s1 = v_cache->stride[1];
   p.vc_s2 = v_cache->stride[2];
   p.num_slots = static_cast<int64_t>(NB) * kBlock;
-  p.k_scale = kv_dtype == PA_KV_FP8_E4M3 ? k_scale : nullptr;
-  p.v_scale = kv_dtype == PA_KV_FP8_E4M3 ? v_scale : nullptr;
-  p.err = device_error;
+  p.k_scale = kv_dtype == PA_KV_FP8_E4M3 ? o.k_scale : nullptr;
+  p.v_scale = kv_dtype == PA_KV_FP8_E4M3 ? o.v_scale : nullptr;
+  p.scale_stride = o.scale_stride;
+  p.err = o.device_error;
   const int sm = device_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -381,6 +393,16 @@ PA_API int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa
     e = launch_write(p, in_dt, k_cache->dtype, sm, st);
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache, pa_tensor *v_cache,
+                                const pa_tensor *slot_mapping, int kv_dtype, const float *k_scale,
+                                const float *v_scale, int *device_error, pa_stream_t stream) {
+  pa_write_options o{};
+  o.k_scale = k_scale;
+  o.v_scale = v_scale;
+  o.device_error = device_error;
+  return pa_reshape_and_cache_opt(key, value, k_cache, v_cache, slot_mapping, kv_dtype, &o, stream);
 }
 
 PA_API int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int max_blocks_per_seq,
@@ -435,8 +457,13 @@ namespace {
 
 int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                 const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
-                const float *k_scale, const float *v_scale, int partition_size, void *workspace,
-                size_t workspace_bytes, bool internal_ws, int *device_error, pa_stream_t stream) {
+                const pa_decode_options &o, bool internal_ws, pa_stream_t stream) {
+  const float *k_scale = o.k_scale, *v_scale = o.v_scale;
+  const int partition_size = o.partition_size;
+  void *workspace = o.workspace;
+  size_t workspace_bytes = o.workspace_bytes;
+  int *device_error = o.device_error;
+  if (o.scale_stride < 0) return PA_ERR_INVALID_ARG;
   int r;
   if ((r = check_desc(out, 3)) || (r = check_desc(q, 3)) || (r = check_desc(block_table, 2)) ||
       (r = check_desc(seq_lens, 1)))
@@ -496,6 +523,8 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   p.scale_log2 = scale * 1.4426950408889634f;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.scale_stride = o.scale_stride;
+  p.alibi = o.alibi_slopes;
   p.pages_per_part = P > 0 ? P / kBlock : std::max(maxNB, 1);
   p.max_parts = max_parts;
   p.cluster = pl.cluster;
@@ -552,7 +581,10 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
     e = launch_decode_f32(p, st);
   } else {
     CUtensorMap tmK, tmV;
-    if ((r = make_cache_map(k_cache, &tmK)) || (r = make_cache_map(v_cache, &tmV))) return r;
+    int nhd_k = 0, nhd_v = 0;
+    if ((r = make_cache_map(k_cache, &tmK, &nhd_k)) || (r = make_cache_map(v_cache, &tmV, &nhd_v))) return r;
+    if (nhd_k != nhd_v) return PA_ERR_INVALID_ARG;  // K and V in different layouts
+    p.nhd = nhd_k;
     ProfScope ps(PA_KERNEL_DECODE, st);
     if (kind == KIND_BF16 || kind == KIND_F16) e = launch_decode_mma_16(p, kind, tmK, tmV, st);
     else e = launch_decode_mma_fp8(p, kind, tmK, tmV, st);
@@ -566,15 +598,29 @@ PA_API int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_c
                         const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
                         const float *k_scale, const float *v_scale, int partition_size, void *workspace,
                         size_t workspace_bytes, int *device_error, pa_stream_t stream) {
-  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, k_scale, v_scale,
-                     partition_size, workspace, workspace_bytes, false, device_error, stream);
+  pa_decode_options o{};
+  o.k_scale = k_scale;
+  o.v_scale = v_scale;
+  o.partition_size = partition_size;
+  o.workspace = workspace;
+  o.workspace_bytes = workspace_bytes;
+  o.device_error = device_error;
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, false, stream);
 }
 
 PA_API int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                      const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
                      pa_stream_t stream) {
-  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, nullptr, nullptr, 0,
-                     nullptr, 0, true, nullptr, stream);
+  const pa_decode_options o{};
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, true, stream);
+}
+
+PA_API int pa_decode_opt(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                         const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                         const pa_decode_options *opt, pa_stream_t stream) {
+  const pa_decode_options o = opt ? *opt : pa_decode_options{};
+  const bool internal = !o.workspace && o.workspace_bytes == 0;
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, internal, stream);
 }
 
 PA_API int pa_check_device_error(int *device_error, int *bits_out, pa_stream_t stream) {

@@ -40,9 +40,11 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
         static_cast<float *>(p.out)[s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D] = 0.f;
     return;
   }
-  float q[8][PER], acc[8][PER], m[8], l[8];
+  float q[8][PER], acc[8][PER], m[8], l[8], ab[8];
 #pragma unroll
   for (int hh = 0; hh < 8; ++hh) {
+    // ALiBi slope in log2 units (0 without ALiBi): logit += slope * (t - (len - 1))
+    ab[hh] = (p.alibi && hh < ng) ? __ldg(p.alibi + h0 + hh) * 1.4426950408889634f : 0.f;
     const int h = h0 + min(hh, ng - 1);
     const float *qr = static_cast<const float *>(p.q) + s * p.q_ss + static_cast<int64_t>(h) * p.q_hs;
 #pragma unroll
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
           for (int i = 0; i < PER; ++i) z = fmaf(q[hh][i], kr[i], z);
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-          z *= p.scale_log2;
+          z = fmaf(ab[hh], static_cast<float>(page * kBlock + t - (len - 1)), z * p.scale_log2);
           const float mn = fmaxf(m[hh], z);
           const float al = ex2(m[hh] - mn);
           const float pz = ex2(z - mn);

@@ -57,6 +57,7 @@ namespace pa {
 
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before a wait gives up (>= ~20 ms)
 constexpr float kMaxSlack = 8.f;            // log2 units: probabilities within a page stay <= 256
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int KIND, int D, int W, int STAGES>
 struct MmaCfg {
@@ -119,11 +120,12 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
       const uint32_t bar = bar0 + 8 * st;
       const uint32_t kdst = stage0 + st * C::STAGEB;
       mbar_arrive_expect_tx(bar, C::STAGEB);
+      const int c1 = p.nhd ? g : 0, c2 = p.nhd ? 0 : g;  // (token, head) or (head, token) order
 #pragma unroll
-      for (int b = 0; b < C::NBOX; ++b) tma_load_4d(kdst + b * 2048, tmK, bar, b * C::BOXE, 0, g, pid, pol);
+      for (int b = 0; b < C::NBOX; ++b) tma_load_4d(kdst + b * 2048, tmK, bar, b * C::BOXE, c1, c2, pid, pol);
 #pragma unroll
       for (int b = 0; b < C::NBOX; ++b)
-        tma_load_4d(kdst + C::PAGEB + b * 2048, tmV, bar, b * C::BOXE, 0, g, pid, pol);
+        tma_load_4d(kdst + C::PAGEB + b * 2048, tmV, bar, b * C::BOXE, c1, c2, pid, pol);
     }
   };
 
@@ -188,7 +190,7 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
         }
       }
     }
-    const float ks = p.k_scale ? __ldg(p.k_scale) : 1.f;
+    const float ks = p.k_scale ? __ldg(p.k_scale + g * p.scale_stride) : 1.f;  // this KV head's
     const float sf0 = __shfl_sync(0xffffffffu, sfac, (2 * qc) * 4);
     const float sf1 = __shfl_sync(0xffffffffu, sfac, (2 * qc + 1) * 4);
     sc0 = p.scale_log2 * ks / sf0;
@@ -202,6 +204,13 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
   for (int t = 0; t < C::KT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const int ra = lane >> 2;  // token row of score fragments (and +8)
+  // ALiBi slopes of the lane's two head columns (log2 units; 0 without ALiBi): the
+  // logit of token t gets slope * (t - (len - 1)).
+  float ab0 = 0.f, ab1 = 0.f;
+  if (p.alibi) {
+    if (2 * qc < ng) ab0 = __ldg(p.alibi + h0 + 2 * qc) * kLog2e;
+    if (2 * qc + 1 < ng) ab1 = __ldg(p.alibi + h0 + 2 * qc + 1) * kLog2e;
+  }
 
   for (int k = 0; k < nmine; ++k) {
     const int u = u0 + k;  // this page's use of the warp's stages
@@ -258,10 +267,12 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
 
     // ---- online softmax (fragment: rows ra, ra+8 = tokens; columns 2qc, 2qc+1 = heads)
     const bool va = ra < nv, vb8 = ra + 8 < nv;
-    const float s0 = va ? (c0[0] + c1[0]) * sc0 : -INFINITY;
-    const float s1 = va ? (c0[1] + c1[1]) * sc1 : -INFINITY;
-    const float s2 = vb8 ? (c0[2] + c1[2]) * sc0 : -INFINITY;
-    const float s3 = vb8 ? (c0[3] + c1[3]) * sc1 : -INFINITY;
+    const float da = static_cast<float>(page * kBlock + ra - (len - 1));  // distance of token ra (<= 0)
+    const float db = da + 8.f;                                             // ... and of token ra + 8
+    const float s0 = va ? fmaf(ab0, da, (c0[0] + c1[0]) * sc0) : -INFINITY;
+    const float s1 = va ? fmaf(ab1, da, (c0[1] + c1[1]) * sc1) : -INFINITY;
+    const float s2 = vb8 ? fmaf(ab0, db, (c0[2] + c1[2]) * sc0) : -INFINITY;
+    const float s3 = vb8 ? fmaf(ab1, db, (c0[3] + c1[3]) * sc1) : -INFINITY;
     // The running max of a head moves only when a score exceeds it by more than
     // kMaxSlack (log2 units); otherwise the page is weighted against the stale max,
     // p = 2^(s - m) <= 2^kMaxSlack, and the cross-lane max reduction and the rescale
@@ -509,7 +520,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
   grid_dependency_wait();
 
   const uint64_t pol = policy_evict_first();
-  const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.f;
+  const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale + g * p.scale_stride) : 1.f;
   float *const smem_w = reinterpret_cast<float *>(sgen);  // merge weights (stage buffers, free by then)
   int used = 0;
   bool stalled = false;

@@ -33,6 +33,7 @@ struct WriteParams {
   int64_t kc_s0, kc_s1, kc_s2, vc_s0, vc_s1, vc_s2; // elements
   int64_t num_slots;                                // num_blocks * 16
   const float *k_scale, *v_scale;                   // nullable
+  int64_t scale_stride;                             // 0: per tensor; else KV head h uses [h * stride]
   int *err;                                         // nullable
 };
 
@@ -47,6 +48,8 @@ struct DecodeParams {
   int num_blocks, max_blocks;
   float scale_log2;                    // softmax scale * log2(e)
   const float *k_scale, *v_scale;      // nullable (1.0)
+  int64_t scale_stride;                // 0: per tensor; else KV head g uses k_scale[g * scale_stride]
+  const float *alibi;                  // nullable: ALiBi slope per query head [Hq]
   int pages_per_part;                  // partition length in pages
   int max_parts;                       // partitions of the longest sequence (1 = unsplit); = cluster if > 1
   int cluster;                         // > 1: cluster split, each unit cut into `cluster` equal parts
@@ -55,6 +58,7 @@ struct DecodeParams {
   float *part_acc;                     // [S, Hq, max_parts, D]
   int *err;                            // nullable
   int lpt;                             // 1: CTA row z takes the z-th longest sequence (S <= kLptMax)
+  int nhd;                             // caches token-major within a block (TMA coordinates (d, g, 0, blk))
   int flat;                            // > 0: balanced split, this many CTAs per head row (S <= kFlatMaxSeqs)
   // fp32 path only: direct cache pointers and strides (elements)
   const float *kc, *vc;

@@ -61,7 +61,9 @@ PA_API int pa_decode_noalloc(pa_tensor *out, const pa_tensor *q, const pa_tensor
   int P = 0, nparts = 1;
   int rc = pa_decode_plan(S, Hq, num_kv_heads, D, max_blocks, k_cache->dtype, 0, partition_size, &P, &nparts);
   if (rc != PA_OK) return rc;
-  const size_t need = P > 0 ? pa_decode_workspace_size(S, Hq, num_kv_heads, D, max_blocks, P) : 0;
+  const size_t need = (P > 0 || P == PA_PARTITION_BALANCED)
+                          ? pa_decode_workspace_size(S, Hq, num_kv_heads, D, max_blocks, P)
+                          : 0;
   if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;  // bigger than the fixed buffer
 
   void *scratch = nullptr;

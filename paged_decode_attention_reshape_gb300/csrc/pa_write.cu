@@ -12,9 +12,10 @@
 // destination (block, head, offset) row is a contiguous run of D * elem bytes in
 // the HND cache, so a warp's stores cover whole 32-byte sectors.  Sources are read
 // once with no L1 allocation.  The grid is at most 8 CTAs per SM, grid-striding
-// over tokens.  The E4M3 path divides by the per-tensor scale with a
-// reciprocal-based, correctly rounded quotient (Divisor below), the same value as
-// an IEEE division.
+// over tokens.  The E4M3 path divides by the tensor's scale, or its KV head's
+// (Part 2: kv_scale_stride == 0 shares one scale, otherwise head h uses
+// scale[h * kv_scale_stride]), with a reciprocal-based, correctly rounded quotient
+// (Divisor below), the same value as an IEEE division.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -155,13 +156,15 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
   const int rows = 256 / width;
   const int tl = threadIdx.x / width;
   const int j0 = threadIdx.x - tl * width;
-  float ks = 1.f, vs = 1.f;
-  if (FP8) {
-    if (p.k_scale) ks = __ldg(p.k_scale);
-    if (p.v_scale) vs = __ldg(p.v_scale);
-  }
-  const Divisor kdiv = make_divisor(ks), vdiv = make_divisor(vs);
   if (tl >= rows) return;  // spare threads when 256 is not a multiple of per_tok
+  // FP8 scales: one per tensor, or one per KV head (head h at [h * scale_stride]).  A
+  // thread's packs belong to one head unless a token is wider than the block.
+  int hcur = j0 / ppr;
+  Divisor kdiv{}, vdiv{};
+  if (FP8) {
+    kdiv = make_divisor(p.k_scale ? __ldg(p.k_scale + hcur * p.scale_stride) : 1.f);
+    vdiv = make_divisor(p.v_scale ? __ldg(p.v_scale + hcur * p.scale_stride) : 1.f);
+  }
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * rows + tl; t < p.T; t += static_cast<int64_t>(gridDim.x) * rows) {
     const int64_t slot = __ldg(p.slot_mapping + t);
     if (slot < 0) continue;  // padding row: no destination
@@ -172,6 +175,11 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteParams p) {
     const int64_t blk = slot / kBlock, off = slot % kBlock;
     for (int j = j0; j < per_tok; j += 256) {
       const int h = j / ppr;
+      if (FP8 && p.scale_stride != 0 && h != hcur) {
+        hcur = h;
+        kdiv = make_divisor(p.k_scale ? __ldg(p.k_scale + h * p.scale_stride) : 1.f);
+        vdiv = make_divisor(p.v_scale ? __ldg(p.v_scale + h * p.scale_stride) : 1.f);
+      }
       const int64_t e = static_cast<int64_t>(j - h * ppr) * EPP;
       const uint4 kv = ld_once(static_cast<const char *>(p.key) + (t * p.key_ts + h * p.key_hs + e) * IB);
       const uint4 vv = ld_once(static_cast<const char *>(p.value) + (t * p.val_ts + h * p.val_hs + e) * IB);

@@ -46,12 +46,18 @@ class Case:
 
 
 def make_case(S, Hq, Hkv, D, lens, dtype=torch.bfloat16, fp8=False, seed=0, k_scale=1.0, v_scale=1.0,
-              extra_blocks=5, table_pad=-1, kv_sigma=1.0, perm=None) -> Case:
+              extra_blocks=5, table_pad=-1, kv_sigma=1.0, perm=None, nhd=False, alibi=None) -> Case:
+    """k_scale / v_scale: one FP8 scale, or Hkv per-head scales.  nhd: caches stored token-major
+    within a block ([NB, 16, Hkv, D]); c.k_cache / c.v_cache are then the [NB, Hkv, 16, D]
+    permuted views.  alibi: per-query-head ALiBi slopes (the reference includes the bias)."""
     assert len(lens) == S
     g = torch.Generator().manual_seed(seed)
     c = Case()
     c.S, c.Hq, c.Hkv, c.D, c.lens = S, Hq, Hkv, D, list(lens)
-    c.dtype, c.fp8, c.k_scale, c.v_scale = dtype, fp8, float(k_scale), float(v_scale)
+    c.dtype, c.fp8 = dtype, fp8
+    c.k_scale = float(k_scale) if np.ndim(k_scale) == 0 else np.asarray(k_scale, dtype=np.float32)
+    c.v_scale = float(v_scale) if np.ndim(v_scale) == 0 else np.asarray(v_scale, dtype=np.float32)
+    c.alibi = None if alibi is None else np.asarray(alibi, dtype=np.float32)
     c.scale = 1.0 / math.sqrt(D)
     nb = [(L + B - 1) // B for L in lens]
     c.NB = sum(nb) + extra_blocks
@@ -69,10 +75,12 @@ def make_case(S, Hq, Hkv, D, lens, dtype=torch.bfloat16, fp8=False, seed=0, k_sc
     c.K = [(torch.randn(L, Hkv, D, generator=g) * kv_sigma).to(kv_dt) for L in lens]
     c.V = [(torch.randn(L, Hkv, D, generator=g) * kv_sigma).to(kv_dt) for L in lens]
     cdt = torch.uint8 if fp8 else dtype
-    c.k_cache = torch.empty((c.NB, Hkv, B, D), dtype=cdt)
-    c.v_cache = torch.empty((c.NB, Hkv, B, D), dtype=cdt)
-    c.k_cache.view(torch.uint8).fill_(0xFF)   # NaN everywhere nothing is written
-    c.v_cache.view(torch.uint8).fill_(0xFF)
+    shape = (c.NB, B, Hkv, D) if nhd else (c.NB, Hkv, B, D)
+    kb, vb = torch.empty(shape, dtype=cdt), torch.empty(shape, dtype=cdt)
+    kb.view(torch.uint8).fill_(0xFF)   # NaN everywhere nothing is written
+    vb.view(torch.uint8).fill_(0xFF)
+    c.k_cache = kb.permute(0, 2, 1, 3) if nhd else kb
+    c.v_cache = vb.permute(0, 2, 1, 3) if nhd else vb
     c.Kval, c.Vval = [], []
     for s, L in enumerate(lens):
         if L == 0:
@@ -103,7 +111,11 @@ def reference(c: Case) -> np.ndarray:
     qd = c.q.double().numpy()
     out = np.zeros((c.S, c.Hq, c.D))
     for s in range(c.S):
-        out[s] = oracle.dense_decode(qd[s], c.Kval[s], c.Vval[s], c.scale)
+        if c.alibi is not None:
+            if c.lens[s] > 0:
+                out[s] = oracle.attention_causal(qd[s][None], c.Kval[s], c.Vval[s], c.scale, c.alibi)[0]
+        else:
+            out[s] = oracle.dense_decode(qd[s], c.Kval[s], c.Vval[s], c.scale)
     return out
 
 
@@ -113,11 +125,17 @@ class OnGpu:
 
 def to_gpu(c: Case, device="cuda") -> OnGpu:
     g = OnGpu()
-    for name in ("q", "k_cache", "v_cache", "block_table", "seq_lens"):
+    for name in ("q", "block_table", "seq_lens"):
         setattr(g, name, getattr(c, name).to(device))
+    for name in ("k_cache", "v_cache"):   # keep the layout (an NHD view stays a view of NHD storage)
+        t = getattr(c, name)
+        base = t.permute(0, 2, 1, 3).contiguous().to(device) if t.stride(2) > t.stride(1) else t.contiguous().to(device)
+        setattr(g, name, base.permute(0, 2, 1, 3) if t.stride(2) > t.stride(1) else base)
     g.out = torch.empty_like(g.q)
-    g.k_scale = torch.tensor([c.k_scale], dtype=torch.float32, device=device)
-    g.v_scale = torch.tensor([c.v_scale], dtype=torch.float32, device=device)
+    g.k_scale = torch.tensor(np.atleast_1d(c.k_scale), dtype=torch.float32, device=device)
+    g.v_scale = torch.tensor(np.atleast_1d(c.v_scale), dtype=torch.float32, device=device)
+    g.scale_stride = 0 if np.ndim(c.k_scale) == 0 else 1
+    g.alibi = None if c.alibi is None else torch.tensor(c.alibi, dtype=torch.float32, device=device)
     g.err = torch.zeros(1, dtype=torch.int32, device=device)
     g.ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)   # zero before first use
     return g
@@ -126,6 +144,11 @@ def to_gpu(c: Case, device="cuda") -> OnGpu:
 def run(c: Case, g: OnGpu, partition_size=0, out=None) -> torch.Tensor:
     import paged_decode_attention_reshape_gb300 as pa
     o = g.out if out is None else out
-    pa.pa_decode_ex(o, g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, c.scale, c.Hkv,
-                    g.k_scale if c.fp8 else None, g.v_scale if c.fp8 else None, partition_size, g.ws, g.err)
+    if g.scale_stride == 0 and g.alibi is None:
+        pa.pa_decode_ex(o, g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, c.scale, c.Hkv,
+                        g.k_scale if c.fp8 else None, g.v_scale if c.fp8 else None, partition_size, g.ws, g.err)
+    else:
+        pa.pa_decode_opt(o, g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, c.scale, c.Hkv,
+                         g.k_scale if c.fp8 else None, g.v_scale if c.fp8 else None, g.scale_stride, g.alibi,
+                         partition_size, g.ws, g.err)
     return o

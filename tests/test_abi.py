@@ -199,3 +199,44 @@ def test_workspace_size(L):
 
 def test_check_device_error_rejects_null(L):
     assert L.pa_check_device_error(None, None, None) == -1
+
+
+def test_option_struct_layouts_match_the_header(tmp_path):
+    """The binding's ctypes structs have the C header's size and field offsets."""
+    import subprocess
+    src = tmp_path / "offsets.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "pa.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu\n", sizeof(pa_write_options), offsetof(pa_write_options, k_scale),
+         offsetof(pa_write_options, v_scale), offsetof(pa_write_options, scale_stride),
+         offsetof(pa_write_options, device_error));
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(pa_decode_options), offsetof(pa_decode_options, k_scale),
+         offsetof(pa_decode_options, v_scale), offsetof(pa_decode_options, scale_stride),
+         offsetof(pa_decode_options, alibi_slopes), offsetof(pa_decode_options, partition_size),
+         offsetof(pa_decode_options, workspace), offsetof(pa_decode_options, workspace_bytes),
+         offsetof(pa_decode_options, device_error));
+  return 0;
+}
+''')
+    exe = tmp_path / "offsets"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.check_call(["gcc", "-I", inc, "-o", str(exe), str(src)])
+    w, d = [list(map(int, l.split())) for l in subprocess.check_output([str(exe)]).decode().split("\n")[:2]]
+    W, D = pa.PaWriteOptions, pa.PaDecodeOptions
+    assert w == [ctypes.sizeof(W)] + [getattr(W, f).offset for f in ("k_scale", "v_scale", "scale_stride",
+                                                                      "device_error")]
+    assert d == [ctypes.sizeof(D)] + [getattr(D, f).offset for f in ("k_scale", "v_scale", "scale_stride",
+                                                                      "alibi_slopes", "partition_size", "workspace",
+                                                                      "workspace_bytes", "device_error")]
+
+
+def test_negative_scale_stride_is_refused(L):
+    o = pa.PaDecodeOptions()
+    o.scale_stride = -1
+    assert L.pa_decode_opt(None, None, None, None, None, None, 1.0, 1, ctypes.byref(o), None) == -1
+    w = pa.PaWriteOptions()
+    w.scale_stride = -2
+    assert L.pa_reshape_and_cache_opt(None, None, None, None, None, 0, ctypes.byref(w), None) == -1

@@ -41,17 +41,23 @@ def oracle_heads(w, s, heads):
         L = K.shape[0]
         ck = np.zeros((L, len(kvh), w.D), dtype=np.uint8)
         cv = np.zeros((L, len(kvh), w.D), dtype=np.uint8)
-        oracle.write_flat(_bits16(K), "bf16", np.arange(L), ck, "e4m3", w.k_scale)
-        oracle.write_flat(_bits16(V), "bf16", np.arange(L), cv, "e4m3", w.v_scale)
-        Kv = oracle.cache_values(ck, "e4m3", w.k_scale)
-        Vv = oracle.cache_values(cv, "e4m3", w.v_scale)
+        ksc = w.k_scales() if np.ndim(w.k_scales()) == 0 else np.asarray(w.k_scales())[kvh]
+        vsc = w.v_scales() if np.ndim(w.v_scales()) == 0 else np.asarray(w.v_scales())[kvh]
+        oracle.write_flat(_bits16(K), "bf16", np.arange(L), ck, "e4m3", ksc)
+        oracle.write_flat(_bits16(V), "bf16", np.arange(L), cv, "e4m3", vsc)
+        Kv = oracle.cache_values(ck, "e4m3", ksc)
+        Vv = oracle.cache_values(cv, "e4m3", vsc)
     else:
         Kv, Vv = K.double().numpy(), V.double().numpy()
     q = data.q(w, "cpu")[s].double().numpy()
     out = []
     for h in heads:
         j = kvh.index(h // w.G)
-        out.append(oracle.dense_decode(q[h][None], Kv[:, j:j + 1], Vv[:, j:j + 1], w.scale)[0])
+        if w.alibi is not None:
+            out.append(oracle.attention_causal(q[h][None, None], Kv[:, j:j + 1], Vv[:, j:j + 1], w.scale,
+                                               w.alibi[h:h + 1])[0, 0])
+        else:
+            out.append(oracle.dense_decode(q[h][None], Kv[:, j:j + 1], Vv[:, j:j + 1], w.scale)[0])
     return np.stack(out)
 
 
@@ -73,7 +79,7 @@ def check_step_write(st, rows=None):
         valid = valid[rows]
     slots = torch.as_tensor(w.step_slot[valid])
     blk, off = slots // B, slots % B
-    for cache, src, scale in ((st.k_cache, st.k_step, w.k_scale), (st.v_cache, st.v_step, w.v_scale)):
+    for cache, src, scale in ((st.k_cache, st.k_step, w.k_scales()), (st.v_cache, st.v_step, w.v_scales())):
         got = cache[blk.cuda(), :, off.cuda(), :].cpu()             # [n, Hkv, D]
         rows_in = src[torch.as_tensor(valid).cuda()].cpu()
         n = len(valid)
@@ -168,3 +174,40 @@ def test_c5_fp8_write_and_sampled_decode():
         assert_close(got[s][heads], oracle_heads(w, int(s), heads), "c5 seq %d" % s)
     # split (the plan) against unsplit on every output
     assert_close(got, step(st, -1), "c5 split vs unsplit")
+
+
+# ---------------------------------------- variants: NHD layout, ALiBi, per-head scales
+
+def test_c2_nhd_full_and_equal_to_hnd():
+    """c2's values in the NHD cache layout: every output against the oracle, and bit-identical
+    to the HND run (same pages, same arithmetic)."""
+    w = configs.get("c2-nhd")
+    st = bench.stage(w)
+    got = step(st, 0)
+    check_step_write(st)
+    for s in range(w.S):
+        assert_close(got[s], oracle_heads(w, s, range(w.Hq)), "c2-nhd seq %d" % s)
+    hnd = bench.stage(configs.get("c2"))
+    assert np.array_equal(got, step(hnd, 0))
+
+
+def test_c3_alibi_sampled():
+    w = configs.get("c3-alibi")
+    st = bench.stage(w)
+    got = step(st, 0)
+    rng = np.random.default_rng(34)
+    for s in rng.choice(w.S, size=6, replace=False):
+        heads = sorted(rng.choice(w.Hq, size=4, replace=False).tolist())
+        assert_close(got[s][heads], oracle_heads(w, int(s), heads), "c3-alibi seq %d" % s)
+
+
+def test_c5_heads_write_and_sampled_decode():
+    w = configs.get("c5-heads")
+    st = bench.stage(w)
+    got = step(st, 0)
+    rng = np.random.default_rng(56)
+    nvalid = int((w.step_slot >= 0).sum())
+    check_step_write(st, rows=np.sort(rng.choice(nvalid, size=512, replace=False)))
+    for s in rng.choice(w.S, size=6, replace=False):
+        heads = sorted(rng.choice(w.Hq, size=3, replace=False).tolist())
+        assert_close(got[s][heads], oracle_heads(w, int(s), heads), "c5-heads seq %d" % s)

@@ -30,6 +30,9 @@ c5  write: 8192 rows = the last 64 positions of 128 sequences, 5% of them
     padding (slot -1; those positions keep their earlier values), bf16 ->
     fp8 e4m3 with k_scale = v_scale = 0.05; decode S=128, 64/8 heads, D=128,
     L ~ U{1024..8192}, pool 1.25x.
+
+Variants with the same values: c2-nhd (NHD cache layout), c3-alibi (ALiBi
+slopes), c5-heads (one FP8 scale per KV head).
 """
 from __future__ import annotations
 
@@ -62,6 +65,17 @@ class Workload:
     step_slot: np.ndarray  # int64 [T]: slot_mapping of the step (-1 = padding)
     outlier_pos: np.ndarray | None = None  # int64 [S] (c4) or None
     notes: dict = field(default_factory=dict)
+    layout: str = "hnd"                    # cache layout: "hnd" [NB, Hkv, 16, D] or "nhd" [NB, 16, Hkv, D]
+    k_head_scales: np.ndarray | None = None  # fp32 [Hkv]: per-head FP8 scales (replace k_scale / v_scale)
+    v_head_scales: np.ndarray | None = None
+    alibi: np.ndarray | None = None        # fp32 [Hq]: ALiBi slopes, or None
+
+    def k_scales(self):
+        """The K quantisation scale(s) the write uses: one float, or [Hkv] per-head scales."""
+        return self.k_scale if self.k_head_scales is None else self.k_head_scales
+
+    def v_scales(self):
+        return self.v_scale if self.v_head_scales is None else self.v_head_scales
 
     @property
     def G(self) -> int:
@@ -217,7 +231,34 @@ def c5() -> Workload:
     return w
 
 
-BUILDERS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5}
+def c2_nhd() -> Workload:
+    """c2 with the caches token-major within a block ([NB, 16, Hkv, D], the NHD layout of
+    "Inside vLLM CUDA Kernels", Part 2); same values."""
+    w = c2()
+    w.name, w.layout = "c2-nhd", "nhd"
+    return w
+
+
+def c3_alibi() -> Workload:
+    """c3 with ALiBi: head h of 32 gets slope 2^(-8 (h + 1) / 32), the usual geometric slopes."""
+    w = c3()
+    w.name = "c3-alibi"
+    w.alibi = (2.0 ** (-8.0 * np.arange(1, w.Hq + 1) / w.Hq)).astype(np.float32)
+    return w
+
+
+def c5_heads() -> Workload:
+    """c5 with one FP8 scale per KV head: K heads 0.04, 0.045, ..., 0.075; V heads the reverse
+    order (|x| / scale stays below 4.5 / 0.04 < 448: no saturation)."""
+    w = c5()
+    w.name = "c5-heads"
+    w.k_head_scales = (0.04 + 0.005 * np.arange(w.Hkv)).astype(np.float32)
+    w.v_head_scales = w.k_head_scales[::-1].copy()
+    return w
+
+
+BUILDERS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5, "c2-nhd": c2_nhd, "c3-alibi": c3_alibi,
+            "c5-heads": c5_heads}
 
 
 def get(name: str) -> Workload:
