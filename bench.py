@@ -104,6 +104,8 @@ def stage(w, device="cuda", history=True, poison=True) -> Staged:
     st.seq_lens = torch.from_numpy(w.seq_lens.astype(np.int32)).to(device)
     st.q = data.q(w, device)
     st.out = torch.empty_like(st.q)
+    # several query tokens per sequence: sequence s owns q / out rows s * nq .. s * nq + nq - 1
+    st.qsl = torch.arange(0, w.S * w.nq + 1, w.nq, dtype=torch.int32, device=device) if w.nq > 1 else None
     st.k_step, st.v_step = data.step_rows(w, device)
     st.slot_mapping = torch.from_numpy(w.step_slot.astype(np.int64)).to(device)
     if history:
@@ -141,8 +143,9 @@ def workspace_for(st: Staged, partition_size: int):
     import paged_decode_attention_reshape_gb300 as pa
     w = st.w
     code = {"f32": pa.PA_F32, "bf16": pa.PA_BF16, "e4m3": pa.PA_FP8_E4M3}[w.cache_dtype]
-    P, nparts = pa.pa_decode_plan(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, code, 0, partition_size)
-    nbytes = pa.pa_decode_workspace_size(w.S, w.Hq, w.Hkv, w.D, w.max_blocks, P) \
+    hq = w.Hq * w.nq   # varlen: query columns count as Hq * max_query_len heads
+    P, nparts = pa.pa_decode_plan(w.S, hq, w.Hkv, w.D, w.max_blocks, code, 0, partition_size)
+    nbytes = pa.pa_decode_workspace_size(w.S, hq, w.Hkv, w.D, w.max_blocks, P) \
         if (P > 0 or P == pa.PA_PARTITION_BALANCED) else 0
     ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=st.q.device)   # zero before first use
     return P, nparts, ws
@@ -157,7 +160,10 @@ def run_decode(st: Staged, partition_size: int = 0, ws=None, out=None) -> None:
     w = st.w
     o = st.out if out is None else out
     ks, vs = (st.k_scale, st.v_scale) if st.fp8 else (None, None)
-    if st.scale_stride or st.alibi is not None:
+    if st.qsl is not None:
+        pa.pa_attention_varlen(o, st.q, st.k_cache, st.v_cache, st.qsl, st.block_table, st.seq_lens, w.scale,
+                               w.Hkv, w.nq, ks, vs, st.scale_stride, st.alibi, partition_size, ws, st.err)
+    elif st.scale_stride or st.alibi is not None:
         pa.pa_decode_opt(o, st.q, st.k_cache, st.v_cache, st.block_table, st.seq_lens, w.scale, w.Hkv, ks, vs,
                          st.scale_stride, st.alibi, partition_size, ws, st.err)
     else:
@@ -301,7 +307,7 @@ def e2e_steps(st, K, flush, partition_size, ws):
     staging buffer (one H2D copy), the library runs on views of it, and the output comes
     back with one D2H copy, all inside the timed events."""
     import copy
-    names = E2E_INPUTS
+    names = E2E_INPUTS + (("qsl",) if st.qsl is not None else ())
     offs, off = {}, 0
     for n in names:
         t = getattr(st, n)
@@ -340,7 +346,7 @@ def cpu_baseline(w, target_s=12.0, max_seqs=None):
     cores = len(os.sched_getaffinity(0))
     rng = np.random.default_rng(7)
     order = rng.permutation(w.S)
-    qs = data.q(w, "cpu").float().double().numpy()
+    qs = data.q(w, "cpu").float().double().numpy().reshape(w.S, w.nq, w.Hq, w.D)
 
     def prep(s):
         K, V = data.logical_kv(w, int(s))
@@ -358,10 +364,10 @@ def cpu_baseline(w, target_s=12.0, max_seqs=None):
             oracle.write_flat(V, "bf16", np.arange(L), cv, "e4m3", w.v_scales())
             K = oracle.cache_values(ck, "e4m3", w.k_scales())
             V = oracle.cache_values(cv, "e4m3", w.v_scales())
-        if w.alibi is not None:
-            oracle.attention_causal(qs[s][None], K, V, w.scale, w.alibi)
+        if w.alibi is not None or w.nq > 1:
+            oracle.attention_causal(qs[s], K, V, w.scale, w.alibi)
         else:
-            oracle.dense_decode(qs[s], K, V, w.scale)
+            oracle.dense_decode(qs[s][0], K, V, w.scale)
         return L
 
     # calibrate on one sequence, then size the sample to about target_s of wall time; a
@@ -386,11 +392,11 @@ def cpu_baseline(w, target_s=12.0, max_seqs=None):
                 break
     dt = time.perf_counter() - t
     nb = sum((int(w.seq_lens[s]) + 15) // 16 for s in sample)
-    bytes_ = nb * 16 * w.Hkv * w.D * w.cache_elem_bytes() * 2 + 2 * n * w.Hq * w.D * w.in_elem_bytes() + nb * 4 + n * 4
+    bytes_ = nb * 16 * w.Hkv * w.D * w.cache_elem_bytes() * 2 + 2 * n * w.nq * w.Hq * w.D * w.in_elem_bytes() + nb * 4 + n * 4
     return {"value": passes * bytes_ / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "%d pass(es) over %d of %d sequences (all %d query heads, fp64 dense decode%s), %.2f s"
                       % (passes, n, w.S, w.Hq, " + e4m3 quantisation" if w.kv_dtype == "e4m3" else "", dt),
-            "tokens_per_s": passes * n / dt}
+            "tokens_per_s": passes * n * w.nq / dt}
 
 
 # --------------------------------------------------------------------- main
@@ -563,7 +569,7 @@ def main(argv=None):
         "config": {"workload": w.name + " " + _workload_desc(w), "l2": "flushed before each step (512 MiB write + 512 MiB read)",
                    "partition_tokens": P, "partitions_max": nparts, "parallelism": "replicas" if ws > 1 else "1 GPU"},
         "pct_of_hbm_peak": 100.0 * value / peak,
-        "tokens_per_s": ws * w.S / (ms * 1e-3),
+        "tokens_per_s": ws * w.S * w.nq / (ms * 1e-3),
         "decode_kernel_us": dk_avg * 1e3,
         "cache_write": {"GB/s": w.write_bytes() / ((wr_ms / max(1, wr_n)) * 1e-3) / 1e9,
                         "kernel_us": wr_ms / max(1, wr_n) * 1e3, "bytes": w.write_bytes()},

@@ -250,6 +250,36 @@ int pa_decode_opt(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, 
                   const pa_decode_options *opt, pa_stream_t stream);
 
 /*
+ * pa_attention_varlen -- paged attention for several new query tokens per sequence
+ * (speculative decoding, chunked prefill): the varlen read path of "Inside vLLM CUDA
+ * Kernels", Part 3 (query_start_loc packs each request's tokens, seq_lens bounds its
+ * visible history, block_table resolves the history's pages).
+ *
+ *   out, q           [Tq, Hq, D]: the new tokens of all sequences, packed; sequence s owns
+ *                    rows query_start_loc[s] .. query_start_loc[s+1]-1 (n_s tokens).  out
+ *                    may not alias q.  Rows of no sequence are not written.
+ *   query_start_loc  PA_I32 [S + 1], non-decreasing (device).
+ *   block_table,     as pa_decode, S rows; seq_lens[s] counts the history and the n_s new
+ *   seq_lens         tokens (already written to the cache).
+ *   max_query_len    host upper bound of every n_s; sizes the grid.
+ * Query i of sequence s sits at position seq_lens[s] - n_s + i and attends to the tokens
+ * 0 .. that position (causal; with alibi_slopes the logit gets slope_h * (t - position)).
+ * n_s = 1 for every s is pa_decode.  A sequence whose rows fall outside [0, Tq), or with
+ * n_s < 0, n_s > max_query_len or n_s > seq_lens[s], writes nothing and sets
+ * PA_DEVERR_SEQLEN_RANGE.
+ * opt: as pa_decode_opt; NULL = defaults.  The partition plan and the workspace size count
+ * query columns as Hq * max_query_len heads: pa_decode_plan / pa_decode_workspace_size
+ * with num_heads = Hq * max_query_len give them.  PA_PARTITION_BALANCED is refused
+ * (PA_ERR_UNSUPPORTED_SHAPE).  Work grows with max_query_len * Hq / Hkv query columns
+ * per KV head, 8 per CTA, each CTA reading the pages its columns see: meant for a few to
+ * a few tens of tokens per sequence.
+ */
+int pa_attention_varlen(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                        const pa_tensor *query_start_loc, const pa_tensor *block_table, const pa_tensor *seq_lens,
+                        float scale, int num_kv_heads, int max_query_len, const pa_decode_options *opt,
+                        pa_stream_t stream);
+
+/*
  * pa_decode_noalloc -- pa_decode_ex for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this call; it exists for callers that have no

@@ -30,7 +30,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED_DTYPE", 
           -8: "PA_ERR_DEVICE_TIMEOUT"}
 
 EXPORTS = ("pa_reshape_and_cache", "pa_reshape_and_cache_opt", "pa_decode", "pa_decode_ex", "pa_decode_opt",
-           "pa_decode_noalloc", "pa_decode_plan", "pa_decode_workspace_size", "pa_check_device_error",
+           "pa_attention_varlen", "pa_decode_noalloc", "pa_decode_plan", "pa_decode_workspace_size", "pa_check_device_error",
            "pa_status_string", "pa_profile_enable", "pa_profile_read")
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 PA_PARTITION_BALANCED = -100  # partition_size: balanced split over one resident wave
@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
             L.pa_reshape_and_cache_opt.argtypes = [T, T, T, T, T, i32, ctypes.POINTER(PaWriteOptions), P]
             L.pa_decode_opt.restype = i32
             L.pa_decode_opt.argtypes = [T, T, T, T, T, T, f32, i32, ctypes.POINTER(PaDecodeOptions), P]
+            L.pa_attention_varlen.restype = i32
+            L.pa_attention_varlen.argtypes = [T, T, T, T, T, T, T, f32, i32, i32, ctypes.POINTER(PaDecodeOptions), P]
             L.pa_decode.restype = i32
             L.pa_decode.argtypes = [T, T, T, T, T, T, f32, i32, P]
             L.pa_decode_ex.restype = i32
@@ -183,6 +185,24 @@ def pa_decode_opt(out, q, k_cache, v_cache, block_table, seq_lens, scale: float,
     rc = lib().pa_decode_opt(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), ctypes.byref(o),
                              _stream(stream))
     _check(rc, "pa_decode_opt")
+
+
+def pa_attention_varlen(out, q, k_cache, v_cache, query_start_loc, block_table, seq_lens, scale: float,
+                        num_kv_heads: int, max_query_len: int, k_scale=None, v_scale=None, scale_stride: int = 0,
+                        alibi_slopes=None, partition_size: int = 0, workspace=None, device_error=None,
+                        stream=None) -> None:
+    """Several new query tokens per sequence: q/out [Tq, Hq, D] packed, sequence s owning rows
+    query_start_loc[s] .. query_start_loc[s+1]-1 (int32 [S+1]); query i of s sits at position
+    seq_lens[s] - n_s + i and sees the tokens up to it.  Options as pa_decode_opt; the workspace
+    size is pa_decode_workspace_size with num_heads = Hq * max_query_len."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    o = PaDecodeOptions(_ptr(k_scale), _ptr(v_scale), int(scale_stride), _ptr(alibi_slopes), int(partition_size),
+                        _ptr(workspace), ws_bytes, _ptr(device_error))
+    args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(query_start_loc), desc(block_table),
+            desc(seq_lens))
+    rc = lib().pa_attention_varlen(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads),
+                                   int(max_query_len), ctypes.byref(o), _stream(stream))
+    _check(rc, "pa_attention_varlen")
 
 
 def pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, num_kv_heads: int,

@@ -455,9 +455,13 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
 
 namespace {
 
+// Decode (query_start_loc == NULL: one query token per sequence, q [S, Hq, D]) or varlen
+// attention (q [Tq, Hq, D] packed, query_start_loc [S + 1], at most max_query_len tokens
+// per sequence).
 int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                 const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
-                const pa_decode_options &o, bool internal_ws, pa_stream_t stream) {
+                const pa_decode_options &o, bool internal_ws, pa_stream_t stream,
+                const pa_tensor *query_start_loc = nullptr, int max_query_len = 1) {
   const float *k_scale = o.k_scale, *v_scale = o.v_scale;
   const int partition_size = o.partition_size;
   void *workspace = o.workspace;
@@ -470,8 +474,18 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
     return r;
   int NB, Hkv, D;
   if ((r = validate_cache_pair(k_cache, v_cache, &NB, &Hkv, &D))) return r;
-  const int64_t S64 = q->shape[0], Hq64 = q->shape[1];
+  const bool varlen = query_start_loc != nullptr;
+  const int64_t S64 = varlen ? seq_lens->shape[0] : q->shape[0], Hq64 = q->shape[1];
   if (num_kv_heads != Hkv || Hkv <= 0 || Hq64 <= 0 || Hq64 % Hkv) return PA_ERR_INVALID_ARG;
+  if (varlen) {
+    if ((r = check_desc(query_start_loc, 1))) return r;
+    if (query_start_loc->dtype != PA_I32) return PA_ERR_UNSUPPORTED_DTYPE;
+    if (query_start_loc->shape[0] != S64 + 1 || query_start_loc->stride[0] != 1 || !query_start_loc->data)
+      return PA_ERR_INVALID_ARG;
+    if (max_query_len < 1) return PA_ERR_INVALID_ARG;
+    if (o.partition_size == PA_PARTITION_BALANCED) return PA_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(max_query_len) * (Hq64 / Hkv) > (1 << 20)) return PA_ERR_UNSUPPORTED_SHAPE;
+  }
   if (q->shape[2] != D) return PA_ERR_INVALID_ARG;
   for (int i = 0; i < 3; ++i)
     if (out->shape[i] != q->shape[i]) return PA_ERR_INVALID_ARG;
@@ -485,7 +499,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED_SHAPE;
   if ((kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) && D < 128) return PA_ERR_UNSUPPORTED_SHAPE;
   if (S64 > 65535 || Hq64 > 65535 || block_table->shape[1] > (INT32_MAX / kBlock)) return PA_ERR_UNSUPPORTED_SHAPE;
-  if (S64 == 0) return PA_OK;
+  if (S64 == 0 || q->shape[0] == 0) return PA_OK;
   if (!q->data || !out->data || !block_table->data || !seq_lens->data) return PA_ERR_INVALID_ARG;
   const int qb = elem_bytes(q->dtype);
   if (!aligned16(q->data) || !aligned16(out->data)) return PA_ERR_ALIGNMENT;
@@ -493,10 +507,14 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
     if ((q->stride[i] * qb) % 16 || (out->stride[i] * qb) % 16) return PA_ERR_ALIGNMENT;
 
   const int S = static_cast<int>(S64), Hq = static_cast<int>(Hq64);
+  // query columns per KV head ("virtual heads"): G for decode, G per query token for varlen;
+  // plans and workspace count them like query heads
+  const int VH = (Hq / Hkv) * (varlen ? max_query_len : 1);
+  const int Hqv = Hkv * VH;
   const int maxNB = static_cast<int>(block_table->shape[1]);
   const int sm = device_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
-  const Plan pl = make_plan(S, Hq, Hkv, D, maxNB, kind, sm, true, partition_size);
+  const Plan pl = make_plan(S, Hqv, Hkv, D, maxNB, kind, sm, true, partition_size);
   if (pl.status != PA_OK) return pl.status;
   const int P = pl.P;
   const int max_parts = pl.cluster > 1 ? pl.cluster : P > 0 ? (maxNB * kBlock + P - 1) / P : 1;
@@ -516,7 +534,11 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
-  p.HG = (p.G + 7) / 8;
+  p.VH = VH;
+  p.HG = (VH + 7) / 8;
+  p.qsl = varlen ? static_cast<const int32_t *>(query_start_loc->data) : nullptr;
+  p.nq_max = varlen ? max_query_len : 1;
+  p.Tq = q->shape[0];
   p.D = D;
   p.num_blocks = NB;
   p.max_blocks = maxNB;
@@ -543,7 +565,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
 
   if ((max_parts > 1 && pl.cluster <= 1) || pl.flat > 0) {
-    const WsLayout lay = workspace_layout(S, Hq, Hkv, D, maxNB, P, pl.flat);
+    const WsLayout lay = workspace_layout(S, Hqv, Hkv, D, maxNB, P, pl.flat);
     if (internal_ws) {
       int dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
@@ -621,6 +643,17 @@ PA_API int pa_decode_opt(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_
   const pa_decode_options o = opt ? *opt : pa_decode_options{};
   const bool internal = !o.workspace && o.workspace_bytes == 0;
   return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, internal, stream);
+}
+
+PA_API int pa_attention_varlen(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                               const pa_tensor *query_start_loc, const pa_tensor *block_table,
+                               const pa_tensor *seq_lens, float scale, int num_kv_heads, int max_query_len,
+                               const pa_decode_options *opt, pa_stream_t stream) {
+  if (!query_start_loc) return PA_ERR_INVALID_ARG;
+  const pa_decode_options o = opt ? *opt : pa_decode_options{};
+  const bool internal = !o.workspace && o.workspace_bytes == 0;
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, internal, stream,
+                     query_start_loc, max_query_len);
 }
 
 PA_API int pa_check_device_error(int *device_error, int *bits_out, pa_stream_t stream) {

@@ -20,8 +20,8 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int s = blockIdx.z, part = blockIdx.x;
   const int g = blockIdx.y / p.HG, hg = blockIdx.y - g * p.HG;
-  const int h0 = g * p.G + hg * 8;
-  const int ng = min(8, p.G - hg * 8);
+  const int v0 = hg * 8;  // first column (virtual head) of this CTA, see DecodeParams
+  int ng = min(8, p.VH - v0);
   const bool split = p.max_parts > 1;
   grid_dependency_wait();
   const int len = __ldg(p.seq_lens + s);
@@ -29,24 +29,40 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
     if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
     return;
   }
-  const int npages = (len + kBlock - 1) / kBlock;
+  int64_t row0 = s;  // the sequence's query tokens: one (decode) or rows qsl[s] .. qsl[s+1]-1
+  int nq = 1;
+  if (p.qsl) {
+    const int a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
+    row0 = a;
+    nq = b - a;
+    if (a < 0 || b > p.Tq || nq < 0 || nq > p.nq_max || nq > len) {  // rows outside q / out, or too many
+      if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
+      return;
+    }
+  }
+  ng = min(ng, nq * p.G - v0);
+  if (ng <= 0) return;
+  const Cols cm{row0, p.G, g, v0};
+  const int pos0 = len - nq;  // column hh sees the tokens up to pos0 + (v0 + hh) / G
+  const int npages = (pos0 + (v0 + ng - 1) / p.G + 1 + kBlock - 1) / kBlock;
   const bool clustered = p.cluster > 1;  // rank `part` of a cluster splitting the unit equally
   const int pb = clustered ? static_cast<int>(static_cast<int64_t>(part) * npages / p.cluster) : part * p.pages_per_part;
   const int pe = clustered ? static_cast<int>(static_cast<int64_t>(part + 1) * npages / p.cluster)
                            : min(npages, pb + p.pages_per_part);
   if (pb >= pe && !clustered) {
     if (!split && part == 0)
-      for (int i = threadIdx.x; i < ng * D; i += W * 32)
-        static_cast<float *>(p.out)[s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D] = 0.f;
+      for (int i = threadIdx.x; i < ng * D; i += W * 32) static_cast<float *>(p.out)[cm.out_off(p, i / D) + i % D] = 0.f;
     return;
   }
   float q[8][PER], acc[8][PER], m[8], l[8], ab[8];
+  int pos[8];
 #pragma unroll
   for (int hh = 0; hh < 8; ++hh) {
-    // ALiBi slope in log2 units (0 without ALiBi): logit += slope * (t - (len - 1))
-    ab[hh] = (p.alibi && hh < ng) ? __ldg(p.alibi + h0 + hh) * 1.4426950408889634f : 0.f;
-    const int h = h0 + min(hh, ng - 1);
-    const float *qr = static_cast<const float *>(p.q) + s * p.q_ss + static_cast<int64_t>(h) * p.q_hs;
+    // last visible position (causal) and ALiBi slope in log2 units (0 without ALiBi):
+    // logit += slope * (t - pos)
+    pos[hh] = hh < ng ? pos0 + (v0 + hh) / p.G : -1;
+    ab[hh] = (p.alibi && hh < ng) ? __ldg(p.alibi + cm.head(hh)) * 1.4426950408889634f : 0.f;
+    const float *qr = static_cast<const float *>(p.q) + cm.q_off(p, min(hh, ng - 1));
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       q[hh][i] = hh < ng ? __ldg(qr + lane + 32 * i) : 0.f;
@@ -74,15 +90,16 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
         kr[i] = __ldg(kbase + t * p.kc_s2 + lane + 32 * i);
         vr[i] = __ldg(vbase + t * p.vc_s2 + lane + 32 * i);
       }
+      const int tt = page * kBlock + t;  // the token's position
 #pragma unroll
       for (int hh = 0; hh < 8; ++hh) {
-        if (hh < ng) {
+        if (tt <= pos[hh]) {  // visible to this column (never for hh >= ng)
           float z = 0.f;
 #pragma unroll
           for (int i = 0; i < PER; ++i) z = fmaf(q[hh][i], kr[i], z);
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-          z = fmaf(ab[hh], static_cast<float>(page * kBlock + t - (len - 1)), z * p.scale_log2);
+          z = fmaf(ab[hh], static_cast<float>(tt - pos[hh]), z * p.scale_log2);
           const float mn = fmaxf(m[hh], z);
           const float al = ex2(m[hh] - mn);
           const float pz = ex2(z - mn);
@@ -126,11 +143,12 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
         if (d == 0) cmd[hh] = make_float2(M, den);
       }
     }
-    cluster_merge_write<float, D>(p, s, h0, ng, 1.f, any_bad, &sm[0][0][0], D + 2, cmd, &cbad, W * 32);
+    cluster_merge_write<float, D>(p, cm, ng, 1.f, any_bad, &sm[0][0][0], D + 2, cmd, &cbad, W * 32);
     return;
   }
   const int nparts = split ? (npages + p.pages_per_part - 1) / p.pages_per_part : 1;
   const bool direct = nparts == 1;
+  const FixedRows rows{(static_cast<int64_t>(s) * p.Hkv + g) * p.VH + v0, p.max_parts};
   if (!any_bad) {
     for (int i = threadIdx.x; i < ng * D; i += W * 32) {
       const int hh = i / D, d = i - hh * D;
@@ -145,12 +163,10 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
         den += sc * sm[w][hh][D + 1];
         num += sc * sm[w][hh][d];
       }
-      const int h = h0 + hh;
       if (direct) {
-        static_cast<float *>(p.out)[s * p.out_ss + static_cast<int64_t>(h) * p.out_hs + d] =
-            den > 0.f ? num / den : 0.f;
+        static_cast<float *>(p.out)[cm.out_off(p, hh) + d] = den > 0.f ? num / den : 0.f;
       } else {
-        const int64_t row = (static_cast<int64_t>(s) * p.Hq + h) * p.max_parts + part;
+        const int64_t row = rows(hh, part);
         p.part_acc[row * D + d] = num;
         if (d == 0) p.part_ml[row] = make_float2(M, den);
       }
@@ -158,8 +174,8 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
   }
   static_assert(sizeof(sm) >= 8 * kMergeSmemParts * 4, "merge weights reuse sm");
   if (!direct)
-    merge_if_last<float, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, 1.f, W * 32,
-                            &sm[0][0][0], FixedRows{static_cast<int64_t>(s) * p.Hq + h0, p.max_parts});
+    merge_if_last<float, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, ng, nparts, 1.f, W * 32,
+                            &sm[0][0][0], rows);
 }
 
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st) {

@@ -58,6 +58,7 @@ namespace pa {
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before a wait gives up (>= ~20 ms)
 constexpr float kMaxSlack = 8.f;            // log2 units: probabilities within a page stay <= 256
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kEmptyMax = -1e30f;         // running max of a column with no visible token yet
 
 template <int KIND, int D, int W, int STAGES>
 struct MmaCfg {
@@ -81,9 +82,10 @@ struct MmaCfg {
   static_assert(kMmaScratch >= (kFlatMaxSeqs + 1) * 4, "balanced-split page offsets");
 };
 
-// Runs pages [pb, pe) of sequence s (length len) for KV head g and the query heads
-// h0 .. h0+ng-1 through the warps' pipelines, and leaves each warp's state at the
-// start of its own stage region: (m, l) per head, then acc[8][D].  `used` counts the
+// Runs pages [pb, pe) of sequence s (length len) for KV head g and the CTA's query
+// columns 0 .. ng-1 (cm; column j sees the tokens up to position pos0 + (v0 + j) / G)
+// through the warps' pipelines, and leaves each warp's state at the start of its own
+// stage region: (m, l) per column, then acc[8][D].  `used` counts the
 // pages this warp has already taken through its stages: the mbarrier phases go on
 // from there, so a CTA can run several ranges in a row.  With `pid_ready`, pid_reg
 // already holds lane i's table entry for the warp's i-th page (read early by the
@@ -92,11 +94,12 @@ struct MmaCfg {
 template <int KIND, int D, int W, int STAGES>
 __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
                                           const uint32_t sbase, uint8_t *const sgen, int &used, bool &stalled,
-                                          const int s, const int len, const int g, const int h0, const int ng,
-                                          const int pb, const int pe, int pid_reg, const bool pid_ready,
-                                          const uint64_t pol) {
+                                          const int s, const int len, const Cols &cm, const int pos0,
+                                          const int ng, const int pb, const int pe, int pid_reg,
+                                          const bool pid_ready, const uint64_t pol) {
   using C = MmaCfg<KIND, D, W, STAGES>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = cm.g;
   const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
   const int nmine = (pe - pb > warp) ? (pe - pb - warp + W - 1) / W : 0;
   const uint32_t stage0 = sbase + static_cast<uint32_t>(warp * STAGES * C::STAGEB);
@@ -135,8 +138,7 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
   // ------------------------------------------------------- query fragments
   const int qh = lane >> 2, qc = lane & 3;  // fragment row (head / token) and column group
   const bool qvalid = qh < ng;
-  const char *qrow = static_cast<const char *>(p.q) +
-                     (static_cast<int64_t>(s) * p.q_ss + static_cast<int64_t>(h0 + (qvalid ? qh : 0)) * p.q_hs) * 2;
+  const char *qrow = static_cast<const char *>(p.q) + cm.q_off(p, qvalid ? qh : 0) * 2;
   uint32_t qf[C::KT][2];
   float sc0, sc1;  // score scale (log2 units) of this lane's two head columns 2qc, 2qc+1
   if constexpr (!C::FP8) {
@@ -202,14 +204,20 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
   float acc[C::KT][4];
 #pragma unroll
   for (int t = 0; t < C::KT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // Running max of an empty column: a finite stand-in for -inf, so a page with every
+  // token masked for a column (a causal column whose tokens end before this warp's first
+  // page) gives p = 2^(-inf - m) = 0, never 2^(-inf + inf).
+  float m0 = kEmptyMax, m1 = kEmptyMax, l0 = 0.f, l1 = 0.f;
   const int ra = lane >> 2;  // token row of score fragments (and +8)
-  // ALiBi slopes of the lane's two head columns (log2 units; 0 without ALiBi): the
-  // logit of token t gets slope * (t - (len - 1)).
+  // The lane's two columns 2qc, 2qc+1: the last visible position (causal; -1 for a column
+  // beyond the CTA's queries) and the ALiBi slope (log2 units; 0 without ALiBi), which
+  // adds slope * (t - position) to the logit of token t.
+  const int posA = 2 * qc < ng ? pos0 + (cm.v0 + 2 * qc) / cm.G : -1;
+  const int posB = 2 * qc + 1 < ng ? pos0 + (cm.v0 + 2 * qc + 1) / cm.G : -1;
   float ab0 = 0.f, ab1 = 0.f;
   if (p.alibi) {
-    if (2 * qc < ng) ab0 = __ldg(p.alibi + h0 + 2 * qc) * kLog2e;
-    if (2 * qc + 1 < ng) ab1 = __ldg(p.alibi + h0 + 2 * qc + 1) * kLog2e;
+    if (2 * qc < ng) ab0 = __ldg(p.alibi + cm.head(2 * qc)) * kLog2e;
+    if (2 * qc + 1 < ng) ab1 = __ldg(p.alibi + cm.head(2 * qc + 1)) * kLog2e;
   }
 
   for (int k = 0; k < nmine; ++k) {
@@ -266,13 +274,11 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
     }
 
     // ---- online softmax (fragment: rows ra, ra+8 = tokens; columns 2qc, 2qc+1 = heads)
-    const bool va = ra < nv, vb8 = ra + 8 < nv;
-    const float da = static_cast<float>(page * kBlock + ra - (len - 1));  // distance of token ra (<= 0)
-    const float db = da + 8.f;                                             // ... and of token ra + 8
-    const float s0 = va ? fmaf(ab0, da, (c0[0] + c1[0]) * sc0) : -INFINITY;
-    const float s1 = va ? fmaf(ab1, da, (c0[1] + c1[1]) * sc1) : -INFINITY;
-    const float s2 = vb8 ? fmaf(ab0, db, (c0[2] + c1[2]) * sc0) : -INFINITY;
-    const float s3 = vb8 ? fmaf(ab1, db, (c0[3] + c1[3]) * sc1) : -INFINITY;
+    const int ta = page * kBlock + ra, tb = ta + 8;  // the fragment's two tokens
+    const float s0 = ta <= posA ? fmaf(ab0, static_cast<float>(ta - posA), (c0[0] + c1[0]) * sc0) : -INFINITY;
+    const float s1 = ta <= posB ? fmaf(ab1, static_cast<float>(ta - posB), (c0[1] + c1[1]) * sc1) : -INFINITY;
+    const float s2 = tb <= posA ? fmaf(ab0, static_cast<float>(tb - posA), (c0[2] + c1[2]) * sc0) : -INFINITY;
+    const float s3 = tb <= posB ? fmaf(ab1, static_cast<float>(tb - posB), (c0[3] + c1[3]) * sc1) : -INFINITY;
     // The running max of a head moves only when a score exceeds it by more than
     // kMaxSlack (log2 units); otherwise the page is weighted against the stale max,
     // p = 2^(s - m) <= 2^kMaxSlack, and the cross-lane max reduction and the rescale
@@ -420,7 +426,7 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
 // (head, element) of the group, writes the normalised output (direct) or stores the
 // CTA's state (m, l, unnormalised acc) in workspace row rows(hh).
 template <int KIND, int D, int W, int STAGES, typename OutT, typename RowFn>
-__device__ __forceinline__ void write_cta_state(const DecodeParams &p, const uint8_t *sgen, int s, int h0, int ng,
+__device__ __forceinline__ void write_cta_state(const DecodeParams &p, const uint8_t *sgen, const Cols &cm, int ng,
                                                 float vs, bool direct, RowFn rows) {
   using C = MmaCfg<KIND, D, W, STAGES>;
   for (int i = threadIdx.x; i < ng * D; i += C::THREADS) {
@@ -441,7 +447,7 @@ __device__ __forceinline__ void write_cta_state(const DecodeParams &p, const uin
       num += sc * ml[16 + hh * D + d];
     }
     if (direct) {
-      OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + hh) * p.out_hs + d;
+      OutT *o = static_cast<OutT *>(p.out) + cm.out_off(p, hh) + d;
       *o = OutT(den > 0.f ? num / den * vs : 0.f);
     } else {
       const int64_t r = rows(hh);
@@ -452,9 +458,9 @@ __device__ __forceinline__ void write_cta_state(const DecodeParams &p, const uin
 }
 
 template <typename OutT>
-__device__ __forceinline__ void zero_rows(const DecodeParams &p, int s, int h0, int ng, int D, int threads) {
+__device__ __forceinline__ void zero_rows(const DecodeParams &p, const Cols &cm, int ng, int D, int threads) {
   for (int i = threadIdx.x; i < ng * D; i += threads) {
-    OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + i / D) * p.out_hs + i % D;
+    OutT *o = static_cast<OutT *>(p.out) + cm.out_off(p, i / D) + i % D;
     *o = OutT(0.f);
   }
 }
@@ -472,8 +478,9 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int part = blockIdx.x;
   const int g = blockIdx.y / p.HG, hg = blockIdx.y - g * p.HG;
-  const int h0 = g * p.G + hg * 8;      // first query head of this CTA
-  const int ng = min(8, p.G - hg * 8);  // query heads in the group
+  const int v0 = hg * 8;                // first column (virtual head) of this CTA
+  const int h0 = g * p.G + v0;          // decode: its first query head
+  int ng = min(8, p.VH - v0);           // columns in the group (fewer for a short query)
   const bool flat = p.flat > 0;
   using OutT = typename std::conditional<C::QBF16, __nv_bfloat16, __half>::type;
 
@@ -489,6 +496,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
   // returns no data, so it may run before the wait on the previous grid.
   if (warp == 0) {
     if (lane == 0) prefetch_l2(p.seq_lens + (flat ? 0 : blockIdx.z));
+    if (lane == 1 && p.qsl) prefetch_l2(p.qsl + (flat ? 0 : blockIdx.z));
     if (flat) {  // CTA c: the table rows (first head row only) and query heads of sequences c, c + CTAs, ...
       for (int z = part; z < p.S; z += p.flat) {
         if (blockIdx.y == 0) {
@@ -510,7 +518,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
         const int32_t *row = p.block_table + static_cast<int64_t>(z) * p.bt_ss;
         for (int pg = pg0 + lane * 32; pg < pg1; pg += 32 * 32) prefetch_l2(row + pg);
       }
-      if (part == 0) {
+      if (part == 0 && !p.qsl) {
         const char *qr = static_cast<const char *>(p.q) +
                          (static_cast<int64_t>(z) * p.q_ss + static_cast<int64_t>(h0) * p.q_hs) * 2;
         if (lane * 128 < ng * D * 2 && p.q_hs == D) prefetch_l2(qr + lane * 128);
@@ -519,6 +527,9 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
   }
   grid_dependency_wait();
 
+  // Pages are read once per CTA: evict them first.  (With several column groups of one KV
+  // head reading the same pages, evict-normal measured 3 % slower on GB300: 4 query tokens
+  // x 256 sequences x 32/8 heads, 395.6 vs 384.3 us.)
   const uint64_t pol = policy_evict_first();
   const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale + g * p.scale_stride) : 1.f;
   float *const smem_w = reinterpret_cast<float *>(sgen);  // merge weights (stage buffers, free by then)
@@ -571,7 +582,8 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
       __syncthreads();
     }
     for (int z = part; z < p.S; z += p.flat)  // empty sequences: zero output rows
-      if (pref[z] == pref[z + 1] && __ldg(p.seq_lens + z) == 0) zero_rows<OutT>(p, z, h0, ng, D, C::THREADS);
+      if (pref[z] == pref[z + 1] && __ldg(p.seq_lens + z) == 0)
+        zero_rows<OutT>(p, Cols{z, p.G, g, v0}, ng, D, C::THREADS);
 
     const int T = pref[p.S];
     const int Ce = min(p.flat, T);  // CTAs with work: every range holds at least one page
@@ -594,22 +606,24 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     for (int x = a; x < b;) {
       const int ps = pref[z], pn = pref[z + 1];
       const int y = min(b, pn);
+      const Cols cm{z, p.G, g, v0};
+      const int zlen = __ldg(p.seq_lens + z);
       bool bad = true;
       if (!dead)
-        bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, __ldg(p.seq_lens + z), g,
-                                            h0, ng, x - ps, y - ps, 0, false, pol);
+        bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, zlen, cm, zlen - 1, ng,
+                                            x - ps, y - ps, 0, false, pol);
       const bool any_bad = __syncthreads_or(bad);
       if (any_bad) dead = __syncthreads_or(stalled) || dead;
       if (x == ps && y == pn) {
-        if (!any_bad) write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, z, h0, ng, vs, true, [](int) { return int64_t{0}; });
+        if (!any_bad) write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, cm, ng, vs, true, [](int) { return int64_t{0}; });
       } else {
         const int j = x == a ? 0 : 1;  // this CTA's first or last range
         if (!any_bad)
-          write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, z, h0, ng, vs, false,
+          write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, cm, ng, vs, false,
                                                     [&](int hh) { return (my_row * 2 + j) * 8 + hh; });
         // a CTA with an error still counts itself, so the unit's counter returns to zero
         const int c0 = owner(ps);
-        merge_if_last<OutT, D>(p, z, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * z, h0, ng, owner(pn - 1) - c0 + 1,
+        merge_if_last<OutT, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * z, ng, owner(pn - 1) - c0 + 1,
                                vs, C::THREADS, smem_w,
                                FlatRows{static_cast<int64_t>(blockIdx.y) * p.flat + c0, range_start(c0) < ps ? 1 : 0});
       }
@@ -642,7 +656,25 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
     return;
   }
-  const int npages = (len + kBlock - 1) / kBlock;
+  // The sequence's query tokens: one (decode), or rows qsl[s] .. qsl[s+1]-1 (varlen), the last
+  // at position len - 1; column j sees the tokens up to pos0 + (v0 + j) / G.
+  int64_t row0 = s;
+  int nq = 1;
+  if (p.qsl) {
+    const int a = __ldg(p.qsl + s), b = __ldg(p.qsl + s + 1);
+    row0 = a;
+    nq = b - a;
+    if (a < 0 || b > p.Tq || nq < 0 || nq > p.nq_max || nq > len) {  // rows outside q / out, or too many
+      if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0 && p.err) atomicOr(p.err, kErrSeqLen);
+      return;
+    }
+  }
+  ng = min(ng, nq * p.G - v0);  // columns past the sequence's last query token are empty
+  if (ng <= 0) return;
+  const Cols cm{row0, p.G, g, v0};
+  const int pos0 = len - nq;
+  const int vis = pos0 + (v0 + ng - 1) / p.G + 1;  // tokens the CTA's last column sees
+  const int npages = (vis + kBlock - 1) / kBlock;
   int pb, pe;
   if (clustered) {
     pb = static_cast<int>(static_cast<int64_t>(part) * npages / p.cluster);
@@ -654,12 +686,12 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     pe = min(npages, pb + p.pages_per_part);
   }
   if (pb >= pe && !clustered) {  // (an empty cluster rank stays: it takes part in the merge)
-    if (!split && part == 0) zero_rows<OutT>(p, s, h0, ng, D, C::THREADS);  // empty sequence
+    if (!split && part == 0) zero_rows<OutT>(p, cm, ng, D, C::THREADS);  // empty sequence
     return;
   }
 
-  const bool bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, g, h0, ng, pb,
-                                                 pe, pid_reg, true, pol);
+  const bool bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, cm, pos0, ng,
+                                                 pb, pe, pid_reg, true, pol);
   const bool any_bad = __syncthreads_or(bad);
 
   if (clustered) {
@@ -686,18 +718,18 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
         if (d == 0) cmd[hh] = make_float2(M, den);
       }
     }
-    cluster_merge_write<OutT, D>(p, s, h0, ng, vs, any_bad, cs, D, cmd, reinterpret_cast<int *>(cmd + 8),
+    cluster_merge_write<OutT, D>(p, cm, ng, vs, any_bad, cs, D, cmd, reinterpret_cast<int *>(cmd + 8),
                                  C::THREADS);
     return;
   }
   const int nparts = split ? (npages + p.pages_per_part - 1) / p.pages_per_part : 1;
   const bool direct = nparts == 1;  // this CTA holds the whole sequence: write the output
-  const FixedRows rows{static_cast<int64_t>(s) * p.Hq + h0, p.max_parts};
+  const FixedRows rows{(static_cast<int64_t>(s) * p.Hkv + g) * p.VH + v0, p.max_parts};
   if (!any_bad)
-    write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, s, h0, ng, vs, direct, [&](int hh) { return rows(hh, part); });
+    write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, cm, ng, vs, direct, [&](int hh) { return rows(hh, part); });
   // a CTA with an error still counts itself, so the unit's counter returns to zero
   if (!direct)
-    merge_if_last<OutT, D>(p, s, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, h0, ng, nparts, vs, C::THREADS,
+    merge_if_last<OutT, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, ng, nparts, vs, C::THREADS,
                            smem_w, rows);
 }
 

@@ -58,11 +58,34 @@ struct DecodeParams {
   float *part_acc;                     // [S, Hq, max_parts, D]
   int *err;                            // nullable
   int lpt;                             // 1: CTA row z takes the z-th longest sequence (S <= kLptMax)
+  // Query columns.  A CTA covers 8 "virtual heads" of one KV head; virtual head v is query
+  // token v / G of its sequence at query head g G + v % G.  Decode: one token per sequence,
+  // VH = G.  Several tokens (varlen): qsl = query_start_loc [S + 1], VH = nq_max * G.
+  const int32_t *qsl;                  // nullable: sequence s owns q / out rows qsl[s] .. qsl[s+1]-1
+  int nq_max;                          // largest number of query tokens per sequence (1 for decode)
+  int64_t Tq;                          // rows of q / out
+  int VH;                              // virtual heads per KV head; HG = ceil(VH / 8)
   int nhd;                             // caches token-major within a block (TMA coordinates (d, g, 0, blk))
   int flat;                            // > 0: balanced split, this many CTAs per head row (S <= kFlatMaxSeqs)
   // fp32 path only: direct cache pointers and strides (elements)
   const float *kc, *vc;
   int64_t kc_s0, kc_s1, kc_s2, vc_s0, vc_s1, vc_s2;
+};
+
+// The query columns of one CTA: virtual heads v0 .. v0+7 of KV head g (see DecodeParams).
+// Column j is query token (v0 + j) / G of the sequence -- q / out row row0 + (v0 + j) / G --
+// at query head g G + (v0 + j) % G.
+struct Cols {
+  int64_t row0;  // q / out row of the sequence's first query token
+  int G, g, v0;
+  __host__ __device__ __forceinline__ int64_t row(int j) const { return row0 + (v0 + j) / G; }
+  __host__ __device__ __forceinline__ int head(int j) const { return g * G + (v0 + j) % G; }
+  __host__ __device__ __forceinline__ int64_t out_off(const DecodeParams &p, int j) const {
+    return row(j) * p.out_ss + static_cast<int64_t>(head(j)) * p.out_hs;
+  }
+  __host__ __device__ __forceinline__ int64_t q_off(const DecodeParams &p, int j) const {
+    return row(j) * p.q_ss + static_cast<int64_t>(head(j)) * p.q_hs;
+  }
 };
 
 // Error bits (mirror PA_DEVERR_* of pa.h).

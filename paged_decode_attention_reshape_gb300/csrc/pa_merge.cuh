@@ -26,9 +26,9 @@ constexpr int kMergeSmemParts = 256;
 
 // Workspace rows of the partial states.  Row r holds (m, l) at part_ml[r] and acc at
 // part_acc[r * D .. r * D + D).
-// Fixed-size partitions: one row per (sequence, query head, partition).
+// Fixed-size partitions: one row per (sequence, KV head, virtual head, partition).
 struct FixedRows {
-  int64_t head0;  // s * Hq + first head of the group
+  int64_t head0;  // (s * Hkv + g) * VH + v0: the unit's first column among all (sequence, column)
   int max_parts;
   __device__ __forceinline__ int64_t operator()(int hh, int i) const { return (head0 + hh) * max_parts + i; }
 };
@@ -45,9 +45,9 @@ struct FlatRows {
 };
 
 // smem_w: shared memory for 8 * kMergeSmemParts floats, free for reuse by now.
-// rows(hh, i): workspace row of head h0 + hh in the unit's i-th part.
+// rows(hh, i): workspace row of column hh in the unit's i-th part; cm maps columns to outputs.
 template <typename OutT, int D, typename Rows>
-__device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int unit, int h0, int ng, int nparts,
+__device__ __forceinline__ void merge_if_last(const DecodeParams &p, const Cols &cm, int unit, int ng, int nparts,
                                               float vs, int threads, float *smem_w, Rows rows) {
   __shared__ int s_last;
   float(*s_w)[kMergeSmemParts] = reinterpret_cast<float(*)[kMergeSmemParts]>(smem_w);  // weight per head, part
@@ -103,7 +103,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int 
       }
       r *= s_w[hh][1];
     }
-    OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + hh) * p.out_hs + d;
+    OutT *o = static_cast<OutT *>(p.out) + cm.out_off(p, hh) + d;
     *o = static_cast<OutT>(r);
   }
 }
@@ -117,7 +117,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeParams &p, int s, int 
 // each CTA's shared memory alive until the others have read it.  No global memory
 // and no workspace are involved.
 template <typename OutT, int D>
-__device__ __forceinline__ void cluster_merge_write(const DecodeParams &p, int s, int h0, int ng, float vs, bool bad,
+__device__ __forceinline__ void cluster_merge_write(const DecodeParams &p, const Cols &cm, int ng, float vs, bool bad,
                                                     const float *cs, int cs_stride, const float2 *cmd, int *cbad,
                                                     int threads) {
   if (threadIdx.x == 0) *cbad = bad ? 1 : 0;
@@ -139,7 +139,7 @@ __device__ __forceinline__ void cluster_merge_write(const DecodeParams &p, int s
         den += w * md.y;
         num += w * ld_dsmem_f32(dsmem_addr(cs + hh * cs_stride + d, j));
       }
-      OutT *o = static_cast<OutT *>(p.out) + s * p.out_ss + static_cast<int64_t>(h0 + hh) * p.out_hs + d;
+      OutT *o = static_cast<OutT *>(p.out) + cm.out_off(p, hh) + d;
       *o = static_cast<OutT>(den > 0.f ? num / den * vs : 0.f);
     }
   }

@@ -61,6 +61,19 @@ def oracle_heads(w, s, heads):
     return np.stack(out)
 
 
+def oracle_rows(w, s, heads):
+    """fp64 oracle outputs [nq, len(heads), D] of sequence s's query tokens (varlen workloads)."""
+    kvh = sorted({h // w.G for h in heads})
+    K, V = data.logical_kv(w, s, kv_heads=kvh)
+    Kv, Vv = K.double().numpy(), V.double().numpy()
+    q = data.q(w, "cpu").double().numpy()[s * w.nq:(s + 1) * w.nq]
+    out = []
+    for h in heads:
+        j = kvh.index(h // w.G)
+        out.append(oracle.attention_causal(q[:, h:h + 1], Kv[:, j:j + 1], Vv[:, j:j + 1], w.scale)[:, 0])
+    return np.stack(out, axis=1)
+
+
 def step(st, P=0):
     Pp, _, ws = bench.workspace_for(st, P)
     bench.run_write(st)
@@ -211,3 +224,18 @@ def test_c5_heads_write_and_sampled_decode():
     for s in rng.choice(w.S, size=6, replace=False):
         heads = sorted(rng.choice(w.Hq, size=3, replace=False).tolist())
         assert_close(got[s][heads], oracle_heads(w, int(s), heads), "c5-heads seq %d" % s)
+
+
+def test_c3_spec4_write_and_sampled_varlen():
+    """4 query tokens per sequence: the step writes each sequence's last 4 positions, and
+    query i attends to the tokens up to its own position."""
+    w = configs.get("c3-spec4")
+    st = bench.stage(w)
+    got = step(st, 0)
+    check_step_write(st)
+    rng = np.random.default_rng(35)
+    for s in rng.choice(w.S, size=6, replace=False):
+        heads = sorted(rng.choice(w.Hq, size=4, replace=False).tolist())
+        ref = oracle_rows(w, int(s), heads)
+        assert_close(got[s * w.nq:(s + 1) * w.nq][:, heads], ref, "c3-spec4 seq %d" % s)
+    assert_close(got, step(st, -1), "plan vs unsplit")

@@ -32,7 +32,8 @@ c5  write: 8192 rows = the last 64 positions of 128 sequences, 5% of them
     L ~ U{1024..8192}, pool 1.25x.
 
 Variants with the same values: c2-nhd (NHD cache layout), c3-alibi (ALiBi
-slopes), c5-heads (one FP8 scale per KV head).
+slopes), c5-heads (one FP8 scale per KV head), c3-spec4 (4 query tokens per
+sequence, varlen attention; the first token's q is c3's).
 """
 from __future__ import annotations
 
@@ -69,6 +70,7 @@ class Workload:
     k_head_scales: np.ndarray | None = None  # fp32 [Hkv]: per-head FP8 scales (replace k_scale / v_scale)
     v_head_scales: np.ndarray | None = None
     alibi: np.ndarray | None = None        # fp32 [Hq]: ALiBi slopes, or None
+    nq: int = 1                            # new query tokens per sequence (> 1: varlen attention)
 
     def k_scales(self):
         """The K quantisation scale(s) the write uses: one float, or [Hkv] per-head scales."""
@@ -112,11 +114,12 @@ class Workload:
 
     def decode_bytes(self) -> int:
         """Algorithmic bytes of one decode call: K+V pages touched once per KV head,
-        plus q, out, the block-table entries read and seq_lens."""
+        plus q, out, the block-table entries read, seq_lens (and query_start_loc)."""
         nb = sum(self.n_blocks_of(s) for s in range(self.S))
         kv = nb * BLOCK * self.Hkv * self.D * self.cache_elem_bytes() * 2
-        qo = 2 * self.S * self.Hq * self.D * self.in_elem_bytes()
-        return kv + qo + nb * 4 + self.S * 4
+        qo = 2 * self.S * self.nq * self.Hq * self.D * self.in_elem_bytes()
+        qsl = (self.S + 1) * 4 if self.nq > 1 else 0
+        return kv + qo + nb * 4 + self.S * 4 + qsl
 
     def write_bytes(self) -> int:
         """Algorithmic bytes of one cache write: valid rows read and written, plus slot_mapping."""
@@ -257,8 +260,20 @@ def c5_heads() -> Workload:
     return w
 
 
+def c3_spec4() -> Workload:
+    """c3 with 4 new query tokens per sequence (speculative decoding: one token plus three
+    draft tokens): the step writes each sequence's last 4 positions and attends causally."""
+    w = c3()
+    w.name, w.nq = "c3-spec4", 4
+    seqs = np.repeat(np.arange(w.S, dtype=np.int64), w.nq)
+    pos = np.concatenate([np.arange(int(L) - w.nq, int(L), dtype=np.int64) for L in w.seq_lens])
+    w.step_seq, w.step_pos = seqs, pos
+    w.step_slot = np.concatenate([w.slot_of(s, pos[s * w.nq:(s + 1) * w.nq]) for s in range(w.S)]).astype(np.int64)
+    return w
+
+
 BUILDERS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5, "c2-nhd": c2_nhd, "c3-alibi": c3_alibi,
-            "c5-heads": c5_heads}
+            "c5-heads": c5_heads, "c3-spec4": c3_spec4}
 
 
 def get(name: str) -> Workload:

@@ -1,6 +1,6 @@
 """Materialise a workload's values on any device (bit-identical everywhere).
 
-* ``q(w)``              [S, Hq, D]
+* ``q(w)``              [S * nq, Hq, D] (nq query tokens per sequence)
 * ``history_rows(w, s)`` K, V rows of positions [0, L_s) of sequence s, as the
                         history written before the measured step
 * ``step_rows(w)``      K, V rows of the measured step [T, Hkv, D]
@@ -26,8 +26,12 @@ def _round(x: torch.Tensor, dtype: str) -> torch.Tensor:
 
 
 def q(w: Workload, device="cpu") -> torch.Tensor:
-    vals = gen.rows(w.seed, "q", range(w.S), [0] * w.S, w.Hq * w.D, device=device)
-    return _round(vals.view(w.S, w.Hq, w.D), w.dtype)
+    """[S * nq, Hq, D]: query token i of sequence s is row s * nq + i (position index i of the
+    sequence's q stream)."""
+    seqs = [s for s in range(w.S) for _ in range(w.nq)]
+    pos = [i for _ in range(w.S) for i in range(w.nq)]
+    vals = gen.rows(w.seed, "q", seqs, pos, w.Hq * w.D, device=device)
+    return _round(vals.view(w.S * w.nq, w.Hq, w.D), w.dtype)
 
 
 def _outlier_rows(w: Workload, s: int) -> torch.Tensor:
