@@ -71,7 +71,8 @@ typedef enum {
     PA_ERR_CUDA = -5,              /* a CUDA runtime/driver call or launch failed */
     PA_ERR_DEVICE_BOUNDS = -6,     /* device error word: slot / block id / length out of range */
     PA_ERR_UNSUPPORTED_SHAPE = -7, /* head_size or block size outside what is built */
-    PA_ERR_DEVICE_TIMEOUT = -8     /* device error word: a bounded wait gave up */
+    PA_ERR_DEVICE_TIMEOUT = -8,    /* device error word: a bounded wait gave up */
+    PA_ERR_NO_BLOCKS = -9          /* block manager: the pool has too few free blocks */
 } pa_status;
 
 /* Bits of the device error word (an int in device memory, owned by the caller). */
@@ -335,6 +336,64 @@ int pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                                 int max_blocks_per_seq, int partition_size);
+
+/*
+ * Block manager -- host bookkeeping of the physical block pool ("tiny-vllm, Part 6:
+ * the block table and physical block lifetime": one free list, blocks taken when a
+ * token is the first of a logical block, all of a sequence's blocks returned when it
+ * ends; "PagedAttention kernel: paged KV cache & block tables": identical blocks can
+ * be shared across sequences).  Pure host code: no device memory, no stream.  One
+ * manager is not thread safe.
+ *
+ * Blocks carry reference counts.  A forked sequence shares its source's blocks; when
+ * a token is appended to a shared block that is not full, that block is first copied
+ * to a fresh one (copy on write): the append reports the (source, destination) block
+ * pair, and the caller copies it on the device (pa_copy_blocks) before writing the
+ * token's K/V.
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* num_blocks physical blocks (ids 0 .. num_blocks-1), sequence ids 0 .. max_seqs-1,
+ * at most max_blocks_per_seq blocks per sequence.  NULL on bad arguments or no memory. */
+pa_block_manager *pa_bm_create(int num_blocks, int max_seqs, int max_blocks_per_seq);
+void pa_bm_destroy(pa_block_manager *m);
+int pa_bm_num_free(const pa_block_manager *m);          /* free blocks; -1 for NULL */
+int pa_bm_block_refs(const pa_block_manager *m, int block);  /* references; -1 if invalid */
+int64_t pa_bm_seq_len(const pa_block_manager *m, int seq);   /* tokens; -1 if not live */
+
+/* Append n_tokens positions to sequence `seq` (it becomes live) and store their cache
+ * slots (block * 16 + offset) in slots_out (host int64 [n_tokens]).  Blocks are taken
+ * from the free list as tokens start new logical blocks.  copy_out (host int64 [2],
+ * required when the sequence's last block is shared and not full) receives the
+ * (source, destination) pair of a copy on write; *n_copies (nullable) gets 0 or 1.
+ * PA_ERR_NO_BLOCKS (nothing changed) when the pool cannot supply the blocks;
+ * PA_ERR_INVALID_ARG for a bad id, a negative count, more than max_blocks_per_seq blocks,
+ * or a missing copy_out. */
+int pa_bm_append(pa_block_manager *m, int seq, int n_tokens, int64_t *slots_out, int64_t *copy_out,
+                 int *n_copies);
+
+/* Sequence dst (not live) starts as a copy of src (live): same length, same blocks,
+ * each block's reference count + 1. */
+int pa_bm_fork(pa_block_manager *m, int src, int dst);
+
+/* Drop all of a sequence's references; blocks nobody references go back to the free
+ * list.  The sequence is no longer live (freeing one that is not live is a no-op). */
+int pa_bm_free(pa_block_manager *m, int seq);
+
+/* Block-table rows and lengths of sequences seqs[0..n-1] into host arrays: row i of
+ * block_table_out (int32, row_stride >= max_blocks_per_seq entries, unused entries -1)
+ * and seq_lens_out[i] (nullable; 0 for a sequence that is not live), ready for a
+ * host-to-device copy and pa_decode. */
+int pa_bm_export(const pa_block_manager *m, const int *seqs, int n, int row_stride, int32_t *block_table_out,
+                 int32_t *seq_lens_out);
+
+/* Copy whole cache blocks on the device: for each row (src, dst) of block_pairs
+ * (PA_I64 [n, 2], contiguous, device), every (kv head, token) row of block src of
+ * k_cache and v_cache ([num_blocks, Hkv, 16, D], any 16-byte-aligned strides, any cache
+ * type) is copied to block dst.  Pairs naming a block outside [0, num_blocks) copy
+ * nothing and set PA_DEVERR_BLOCK_RANGE.  Asynchronous on `stream`. */
+int pa_copy_blocks(pa_tensor *k_cache, pa_tensor *v_cache, const pa_tensor *block_pairs, int *device_error,
+                   pa_stream_t stream);
 
 /*
  * pa_check_device_error -- synchronise `stream`, read the device error word,

@@ -27,11 +27,13 @@ PA_KERNEL_WRITE, PA_KERNEL_DECODE = 0, 1
 PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_SEQLEN_RANGE, PA_DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
 STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED_DTYPE", -3: "PA_ERR_ALIGNMENT",
           -4: "PA_ERR_WORKSPACE", -5: "PA_ERR_CUDA", -6: "PA_ERR_DEVICE_BOUNDS", -7: "PA_ERR_UNSUPPORTED_SHAPE",
-          -8: "PA_ERR_DEVICE_TIMEOUT"}
+          -8: "PA_ERR_DEVICE_TIMEOUT", -9: "PA_ERR_NO_BLOCKS"}
 
 EXPORTS = ("pa_reshape_and_cache", "pa_reshape_and_cache_opt", "pa_decode", "pa_decode_ex", "pa_decode_opt",
            "pa_attention_varlen", "pa_decode_noalloc", "pa_decode_plan", "pa_decode_workspace_size", "pa_check_device_error",
-           "pa_status_string", "pa_profile_enable", "pa_profile_read")
+           "pa_status_string", "pa_profile_enable", "pa_profile_read", "pa_bm_create", "pa_bm_destroy",
+           "pa_bm_num_free", "pa_bm_block_refs", "pa_bm_seq_len", "pa_bm_append", "pa_bm_fork", "pa_bm_free",
+           "pa_bm_export", "pa_copy_blocks")
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 PA_PARTITION_BALANCED = -100  # partition_size: balanced split over one resident wave
 
@@ -91,6 +93,28 @@ def lib() -> ctypes.CDLL:
             L.pa_decode_opt.argtypes = [T, T, T, T, T, T, f32, i32, ctypes.POINTER(PaDecodeOptions), P]
             L.pa_attention_varlen.restype = i32
             L.pa_attention_varlen.argtypes = [T, T, T, T, T, T, T, f32, i32, i32, ctypes.POINTER(PaDecodeOptions), P]
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            L.pa_bm_create.restype = P
+            L.pa_bm_create.argtypes = [i32, i32, i32]
+            L.pa_bm_destroy.restype = None
+            L.pa_bm_destroy.argtypes = [P]
+            L.pa_bm_num_free.restype = i32
+            L.pa_bm_num_free.argtypes = [P]
+            L.pa_bm_block_refs.restype = i32
+            L.pa_bm_block_refs.argtypes = [P, i32]
+            L.pa_bm_seq_len.restype = ctypes.c_int64
+            L.pa_bm_seq_len.argtypes = [P, i32]
+            L.pa_bm_append.restype = i32
+            L.pa_bm_append.argtypes = [P, i32, i32, i64p, i64p, ctypes.POINTER(i32)]
+            L.pa_bm_fork.restype = i32
+            L.pa_bm_fork.argtypes = [P, i32, i32]
+            L.pa_bm_free.restype = i32
+            L.pa_bm_free.argtypes = [P, i32]
+            L.pa_bm_export.restype = i32
+            L.pa_bm_export.argtypes = [P, ctypes.POINTER(i32), i32, i32, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int32)]
+            L.pa_copy_blocks.restype = i32
+            L.pa_copy_blocks.argtypes = [T, T, T, P, P]
             L.pa_decode.restype = i32
             L.pa_decode.argtypes = [T, T, T, T, T, T, f32, i32, P]
             L.pa_decode_ex.restype = i32
@@ -275,3 +299,73 @@ def pa_profile_read(kind: int):
     ms, n = ctypes.c_double(0), ctypes.c_longlong(0)
     _check(lib().pa_profile_read(int(kind), ctypes.byref(ms), ctypes.byref(n)), "pa_profile_read")
     return ms.value, n.value
+
+
+class BlockManager:
+    """The C block manager (pa_bm_*): free list, per-sequence block tables, reference-counted
+    prefix sharing with copy on write.  Host only."""
+
+    def __init__(self, num_blocks: int, max_seqs: int, max_blocks_per_seq: int):
+        self._m = lib().pa_bm_create(int(num_blocks), int(max_seqs), int(max_blocks_per_seq))
+        if not self._m:
+            raise PAError(-1, "pa_bm_create")
+        self.max_blocks_per_seq = int(max_blocks_per_seq)
+
+    def close(self):
+        if self._m:
+            lib().pa_bm_destroy(self._m)
+            self._m = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return lib().pa_bm_num_free(self._m)
+
+    def refs(self, block: int) -> int:
+        return lib().pa_bm_block_refs(self._m, int(block))
+
+    def seq_len(self, seq: int) -> int:
+        return lib().pa_bm_seq_len(self._m, int(seq))
+
+    def append(self, seq: int, n_tokens: int):
+        """(slots int64 [n_tokens], copy pair (src, dst) or None)."""
+        import numpy as np
+        slots = np.zeros(max(int(n_tokens), 1), dtype=np.int64)
+        pair = np.zeros(2, dtype=np.int64)
+        nc = ctypes.c_int(0)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        rc = lib().pa_bm_append(self._m, int(seq), int(n_tokens), slots.ctypes.data_as(i64p),
+                                pair.ctypes.data_as(i64p), ctypes.byref(nc))
+        _check(rc, "pa_bm_append")
+        return slots[:int(n_tokens)], ((int(pair[0]), int(pair[1])) if nc.value else None)
+
+    def fork(self, src: int, dst: int) -> None:
+        _check(lib().pa_bm_fork(self._m, int(src), int(dst)), "pa_bm_fork")
+
+    def free(self, seq: int) -> None:
+        _check(lib().pa_bm_free(self._m, int(seq)), "pa_bm_free")
+
+    def export(self, seqs, row_stride: int | None = None):
+        """(block_table int32 [n, row_stride], seq_lens int32 [n]) as numpy arrays."""
+        import numpy as np
+        seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+        rs = self.max_blocks_per_seq if row_stride is None else int(row_stride)
+        bt = np.zeros((len(seqs), rs), dtype=np.int32)
+        sl = np.zeros(len(seqs), dtype=np.int32)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        rc = lib().pa_bm_export(self._m, seqs.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), len(seqs), rs,
+                                bt.ctypes.data_as(i32p), sl.ctypes.data_as(i32p))
+        _check(rc, "pa_bm_export")
+        return bt, sl
+
+
+def pa_copy_blocks(k_cache, v_cache, block_pairs, device_error=None, stream=None) -> None:
+    """Copy whole cache blocks: for each row (src, dst) of block_pairs (int64 [n, 2] on the
+    device), block src of k_cache / v_cache is copied to block dst."""
+    args = (desc(k_cache), desc(v_cache), desc(block_pairs))
+    rc = lib().pa_copy_blocks(*[ctypes.byref(a) for a in args], _ptr(device_error), _stream(stream))
+    _check(rc, "pa_copy_blocks")

@@ -323,6 +323,7 @@ PA_API const char *pa_status_string(int status) {
     case PA_ERR_DEVICE_BOUNDS: return "device reported an out-of-range slot, block id or sequence length";
     case PA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (block size, head size or extent)";
     case PA_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case PA_ERR_NO_BLOCKS: return "block pool has too few free blocks";
     default: return "unknown status";
   }
 }
