@@ -57,7 +57,7 @@ class L2Flush:
         self.w.zero_()
         self.r.sum()
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma16.cu", "pa_decode_mma_fp8.cu", "pa_decode.cu",
-                  "pa_device.cuh", "pa_internal.h", "pa_api.cu"]
+                  "pa_device.cuh", "pa_internal.h", "pa_merge.cuh", "pa_api.cu"]
 
 
 # ----------------------------------------------------------------- staging
