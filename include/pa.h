@@ -1,7 +1,7 @@
 /*
  * pa.h -- C ABI of the GB300 paged KV-cache library (libpa_gb300.so).
  *
- * Two operations from the paged-attention pages, plus the plumbing around them:
+ * The paged-attention operations of the pages, plus the plumbing around them:
  *
  *   pa_reshape_and_cache   write each new token's K/V rows into the physical
  *                          cache block its slot_mapping entry names
@@ -12,6 +12,13 @@
  *                          softmax and split-KV partitions merged by a
  *                          log-sum-exp reduce ("Inside vLLM CUDA Kernels", Part 3;
  *                          "vLLM 源码完全拆解（七）", 参数与内存布局 through V1 与 V2)
+ *
+ *   pa_attention_varlen    several new query tokens per sequence, causal
+ *                          ("Inside vLLM CUDA Kernels", Part 3, the varlen read path)
+ *   pa_*_opt               the same calls with per-head FP8 scales and ALiBi
+ *   pa_bm_*, pa_copy_blocks  host block manager and device block copy ("tiny-vllm,
+ *                          Part 6"; "PagedAttention kernel: paged KV cache & block
+ *                          tables")
  *
  * Conventions shared by every call
  * --------------------------------

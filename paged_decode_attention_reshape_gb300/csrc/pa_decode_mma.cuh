@@ -5,10 +5,14 @@
 // over the first seq_lens[s] tokens, reading token t of KV head h / G from
 // physical block block_table[s][t / 16], offset t % 16.
 //
-// Work unit (one CTA): sequence s, KV head g, a group of up to 8 of its query
-// heads, and one split-KV partition of pages.  All query heads of the group share
-// every K/V page the CTA loads, so each page is read from HBM once per KV head,
-// not once per query head.
+// Work unit (one CTA): sequence s, KV head g, a group of 8 query columns, and one
+// split-KV partition of pages.  A column is a "virtual head": for single-query
+// decode one of the KV head's query heads; with several query tokens per sequence
+// (the varlen read path of "Inside vLLM CUDA Kernels", Part 3), column v is query
+// token v / G at head g G + v % G, and sees the tokens up to its own position
+// (causal, the new tokens at the end of the history).  All columns of the group
+// share every K/V page the CTA loads, so each page is read once per KV head (and
+// column group), not once per query head.
 //
 // Inside a CTA, warp w takes pages w, w+W, w+2W, ... of the partition and runs its
 // own pipeline: lane 0 resolves the physical block through block_table and issues
@@ -18,12 +22,14 @@
 // page of the HND cache is 16 rows x D elements; TMA writes it with the 128-byte
 // swizzle so the tensor-core fragment loads below are bank-conflict free.
 //
-// Per 16-token page and the warp's 8-wide head group:
-//   scores  S[16 tok x 8 heads] = K_page[16 x D] . Q^T[D x 8]     (mma m16n8k16, fp32 acc)
-//   online softmax per head (log2 domain): running max m, rescale alpha, p = 2^(s-m),
-//           partial row sums kept per lane and reduced once at the end;
-//           tokens t >= seq_len get -inf (never in the max or the denominator)
-//   output  O^T[D x 8 heads] += V_page^T[D x 16 tok] . P^T[16 tok x 8 heads]
+// Per 16-token page and the CTA's 8 columns:
+//   scores  S[16 tok x 8 cols] = K_page[16 x D] . Q^T[D x 8]      (mma m16n8k16, fp32 acc)
+//           (+ the ALiBi bias slope_h * (t - position), one FMA per score)
+//   online softmax per column (log2 domain): running max m, moved only when a score
+//           exceeds it by more than 2^8 (otherwise the stale max is kept and p <= 256),
+//           p = 2^(s-m), partial row sums kept per lane and reduced once at the end;
+//           tokens a column cannot see get -inf (never in the max or the denominator)
+//   output  O^T[D x 8 cols] += V_page^T[D x 16 tok] . P^T[16 tok x 8 cols]
 //           with P split into hi + lo halves of the 16-bit type (two mmas), so the
 //           probabilities keep ~16 bits; V rows t >= seq_len are zeroed before the
 //           product, so stale or NaN tail values never reach the output.
@@ -34,7 +40,7 @@
 // f16 tensor-core path is used; the query is scaled by a power of two per head so
 // that its largest element lies in [2^14, 2^15) and rounded to f16 (exact for a
 // bf16 query in that range); the power of two and k_scale are folded into the
-// score scale, v_scale into the final output.  K fragments use a permuted
+// score scale, v_scale into the final output (per KV head with per-head scales).  K fragments use a permuted
 // head-dimension order (each lane reads 32 contiguous bytes of a row) and the
 // query uses the same permutation, which leaves q . k unchanged.
 //
@@ -42,7 +48,8 @@
 // region; the CTA merges the W warp states with max/LSE rescaling and writes
 // either the normalised output (a sequence with a single partition) or the
 // partition's state to the workspace, where the unit's last CTA merges all
-// partitions (pa_merge.cuh).
+// partitions (pa_merge.cuh); a cluster split merges through distributed shared
+// memory instead, and the balanced split runs several page ranges per CTA.
 //
 // The kernel is launched as a programmatic dependent of the previous grid on the
 // stream: it waits for that grid before its first global read, so its launch
