@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
   const int pe = clustered ? static_cast<int>(static_cast<int64_t>(part + 1) * npages / p.cluster)
                            : min(npages, pb + p.pages_per_part);
   if (pb >= pe && !clustered) {
-    if (!split && part == 0)
+    if (npages == 0 && part == 0)  // empty sequence (any split): zero output rows
       for (int i = threadIdx.x; i < ng * D; i += W * 32) static_cast<float *>(p.out)[cm.out_off(p, i / D) + i % D] = 0.f;
     return;
   }

@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     pe = min(npages, pb + p.pages_per_part);
   }
   if (pb >= pe && !clustered) {  // (an empty cluster rank stays: it takes part in the merge)
-    if (!split && part == 0) zero_rows<OutT>(p, cm, ng, D, C::THREADS);  // empty sequence
+    if (npages == 0 && part == 0) zero_rows<OutT>(p, cm, ng, D, C::THREADS);  // empty sequence (any split)
     return;
   }
 

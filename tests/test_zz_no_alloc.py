@@ -30,7 +30,7 @@ def _lib():
 
 
 def _noalloc(c, g, partition_size):
-    out = torch.empty_like(g.q)
+    out = torch.full_like(g.q, float("nan"))   # every output must be written by the call
     pa.pa_decode_noalloc(out, g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, c.scale, c.Hkv,
                          g.k_scale if c.fp8 else None, g.v_scale if c.fp8 else None, partition_size, g.err)
     torch.cuda.synchronize()
