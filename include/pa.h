@@ -278,9 +278,12 @@ int pa_decode_opt(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, 
  * opt: as pa_decode_opt; NULL = defaults.  The partition plan and the workspace size count
  * query columns as Hq * max_query_len heads: pa_decode_plan / pa_decode_workspace_size
  * with num_heads = Hq * max_query_len give them.  PA_PARTITION_BALANCED is refused
- * (PA_ERR_UNSUPPORTED_SHAPE).  Work grows with max_query_len * Hq / Hkv query columns
- * per KV head, 8 per CTA, each CTA reading the pages its columns see: meant for a few to
- * a few tens of tokens per sequence.
+ * (PA_ERR_UNSUPPORTED_SHAPE).  Kernels: with fewer than 64 query columns per KV head
+ * (max_query_len * Hq / Hkv), an fp8 or fp32 cache, D other than 64 / 128, or a split
+ * asked for (partition_size > 0 or a cluster split), the decode kernels run with 8
+ * columns per CTA, each CTA reading the pages its columns see.  Otherwise (bf16 / f16
+ * cache, partition_size 0 or -1) a query-tile kernel runs: 64 query rows per CTA share
+ * each page load, the page range is not split and no workspace is used.
  */
 int pa_attention_varlen(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                         const pa_tensor *query_start_loc, const pa_tensor *block_table, const pa_tensor *seq_lens,

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa_gb300.so")
 SOURCES = ["pa_api.cu", "pa_write.cu", "pa_decode.cu", "pa_decode_mma16.cu", "pa_decode_mma_fp8.cu",
-           "pa_noalloc.cu", "pa_blocks.cu"]
+           "pa_noalloc.cu", "pa_blocks.cu", "pa_chunk_mma16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
            "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-warn-spills"]

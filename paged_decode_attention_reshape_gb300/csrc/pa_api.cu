@@ -515,7 +515,11 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   const int maxNB = static_cast<int>(block_table->shape[1]);
   const int sm = device_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
-  const Plan pl = make_plan(S, Hqv, Hkv, D, maxNB, kind, sm, true, partition_size);
+  // Chunks of query tokens run on the query-tile kernel (rows in the MMA M dimension, pages
+  // shared by 64 rows, no split) unless a split was asked for.
+  const bool chunk = varlen && (kind == KIND_BF16 || kind == KIND_F16) && (D == 64 || D == 128) &&
+                     (partition_size == 0 || partition_size == -1) && VH >= kChunkMinColumns;
+  const Plan pl = make_plan(S, Hqv, Hkv, D, maxNB, kind, sm, true, chunk ? -1 : partition_size);
   if (pl.status != PA_OK) return pl.status;
   const int P = pl.P;
   const int max_parts = pl.cluster > 1 ? pl.cluster : P > 0 ? (maxNB * kBlock + P - 1) / P : 1;
@@ -609,7 +613,8 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
     if (nhd_k != nhd_v) return PA_ERR_INVALID_ARG;  // K and V in different layouts
     p.nhd = nhd_k;
     ProfScope ps(PA_KERNEL_DECODE, st);
-    if (kind == KIND_BF16 || kind == KIND_F16) e = launch_decode_mma_16(p, kind, tmK, tmV, st);
+    if (chunk) e = launch_chunk_mma(p, kind, tmK, tmV, st);
+    else if (kind == KIND_BF16 || kind == KIND_F16) e = launch_decode_mma_16(p, kind, tmK, tmV, st);
     else e = launch_decode_mma_fp8(p, kind, tmK, tmV, st);
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

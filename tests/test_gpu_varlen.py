@@ -192,3 +192,53 @@ def test_host_side_refusals():
     with pytest.raises(pa.PAError) as e:
         run(v, g, -1)
     assert e.value.status == -1
+
+
+CHUNK_SHAPES = [
+    # (Hq, Hkv, D, q dtype, alibi): query-tile kernel (>= 32 query columns per KV head)
+    (32, 8, 128, torch.bfloat16, False),
+    (32, 8, 64, torch.float16, False),
+    (8, 8, 128, torch.bfloat16, True),      # MHA: one row per query token
+    (40, 8, 128, torch.bfloat16, True),     # G = 5: 64-row tiles cut tokens apart
+]
+
+
+@pytest.mark.parametrize("shape", CHUNK_SHAPES,
+                         ids=["Hq%d_Hkv%d_D%d_%s%s" % (s[0], s[1], s[2], str(s[3]).split(".")[-1],
+                                                       "_alibi" if s[4] else "") for s in CHUNK_SHAPES])
+def test_long_chunks_match_oracle(shape):
+    """Chunked prefill: up to 192 new tokens over histories of up to 2100 tokens (many
+    64-row query tiles, ragged last tile and page); the same result unsplit, by the
+    heuristic and split into 64-token partitions (the column-group kernels)."""
+    Hq, Hkv, D, dt, alibi = shape
+    slopes = 2.0 ** (-8.0 * np.arange(1, Hq + 1) / Hq) if alibi else None
+    lens, nqs = [1200, 700, 2100, 64, 5], [192, 100, 64, 64, 1]
+    v = make_varlen(lens, nqs, Hq, Hkv, D, dtype=dt, seed=3 * Hq + D, alibi=slopes)
+    ref = reference(v)
+    g = on_gpu(v)
+    outs = {}
+    for P in (-1, 0, 64):
+        got = run(v, g, P)
+        rc, bits = pa.pa_check_device_error(g.err)
+        assert rc == 0, (P, rc, bits)
+        outs[P] = got.clone()
+        got = got.double().cpu().numpy()
+        assert not np.isnan(got).any(), P
+        assert_close(got, ref, "chunk partition %d" % P)
+    assert torch.equal(outs[0], outs[-1])
+    assert_close(outs[64].double().cpu().numpy(), outs[-1].double().cpu().numpy(), "split 64 vs unsplit")
+
+
+def test_query_tile_bad_ranges_are_reported_and_skipped():
+    lens = [50, 40, 30]
+    v = make_varlen(lens, [3, 17, 2], 32, 8, 64, seed=33, nq_max=16)  # 64 columns; sequence 1 > nq_max
+    g = on_gpu(v)
+    ref = reference(v)
+    got = run(v, g, -1)
+    rc, bits = pa.pa_check_device_error(g.err)
+    assert rc == -6 and bits & pa.PA_DEVERR_SEQLEN_RANGE
+    got = got.double().cpu().numpy()
+    a1, b1 = int(v.qsl[1]), int(v.qsl[2])
+    assert np.isnan(got[a1:b1]).all()
+    assert_close(got[:a1], ref[:a1], "sequence 0")
+    assert_close(got[b1:], ref[b1:], "sequence 2")
