@@ -282,8 +282,9 @@ int pa_decode_opt(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, 
  * (max_query_len * Hq / Hkv), an fp8 or fp32 cache, D other than 64 / 128, or a split
  * asked for (partition_size > 0 or a cluster split), the decode kernels run with 8
  * columns per CTA, each CTA reading the pages its columns see.  Otherwise (bf16 / f16
- * cache, partition_size 0 or -1) a query-tile kernel runs: 64 query rows per CTA share
- * each page load, the page range is not split and no workspace is used.
+ * cache, partition_size 0 or -1) a query-tile kernel runs on the tcgen05 tensor cores:
+ * 128 query rows per CTA share each page load, the page range is not split and no
+ * workspace is used.
  */
 int pa_attention_varlen(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                         const pa_tensor *query_start_loc, const pa_tensor *block_table, const pa_tensor *seq_lens,

@@ -613,7 +613,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
     if (nhd_k != nhd_v) return PA_ERR_INVALID_ARG;  // K and V in different layouts
     p.nhd = nhd_k;
     ProfScope ps(PA_KERNEL_DECODE, st);
-    if (chunk) e = launch_chunk_mma(p, kind, tmK, tmV, st);
+    if (chunk) e = launch_chunk_umma(p, kind, tmK, tmV, st);
     else if (kind == KIND_BF16 || kind == KIND_F16) e = launch_decode_mma_16(p, kind, tmK, tmV, st);
     else e = launch_decode_mma_fp8(p, kind, tmK, tmV, st);
   }

@@ -1,0 +1,476 @@
+// pa_chunk_umma.cuh -- paged attention for chunks of query tokens on the 5th-generation
+// tensor cores (tcgen05.mma, accumulators in tensor memory).
+//
+// What it computes is pa_attention_varlen's definition ("Inside vLLM CUDA Kernels",
+// Part 3, FlashAttention over paged KV: a CTA owns a Q tile, resolves and loads the K/V
+// tiles of its sequence through block_table while scanning the K dimension, and runs
+// QK, online softmax and P.V on each): query i of a sequence with n new tokens sits at
+// position len - n + i and sees the tokens up to it; the logit is scale q.k (+ the ALiBi
+// bias slope_h (t - position)).
+//
+// Work unit (one CTA): sequence s, KV head g and 128 query rows -- row r of the KV head
+// is query token r / G at head g G + r % G.  The page range is scanned in groups of 4
+// pages (64 tokens):
+//   S[128 x 64] = Q[128 x D] . K_group^T        tcgen05.mma, A and B from shared memory,
+//                                               S in tensor memory (TMEM)
+//   softmax, one thread per row                 tcgen05.ld of the row's 64 scores; lazy
+//                                               running max; P written back over S as
+//                                               16-bit hi + lo halves (tcgen05.st)
+//   O[128 x D] += P[128 x 16] . V_page[16 x D]  tcgen05.mma per page and half, A = P from
+//                                               TMEM, B = the V page in shared memory
+// Roles (192 threads): warps 0-3 run the softmax and the epilogue (warp w owns TMEM lanes
+// and rows 32 w .. 32 w + 31), warp 4 allocates TMEM and its lane 0 issues the MMAs,
+// warp 5 resolves block_table and issues the TMA page loads into a ring of R page slots.
+// Shared memory holds Q (loaded by the softmax threads, 128-byte swizzle) and the K and V
+// rings, one region per 64-element box of a row, so that the 16-token pages of a group
+// sit at one 1024-byte stride per 8 rows and form one MMA operand.  S and P of groups k
+// and k + 1 use two TMEM buffers; O lives in TMEM until the epilogue normalises it.
+//
+// Synchronisation (mbarriers, every wait bounded and abandoned when another role gave
+// up): full[slot] (TMA bytes) -> MMA; s_full[b] (commit) -> softmax; p_full[b] (128
+// arrivals) -> MMA; o_done (commit after each group's P.V) -> softmax, which waits for
+// every group in turn (an O rescale needs it, and the parity waits stay one phase apart);
+// empty[slot] (commit) -> TMA.  MMAs issued by one thread run in order, so S of group
+// k + 2 may overwrite the P that P.V of group k reads.
+#pragma once
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_merge.cuh"  // grid_dependency_wait
+
+namespace pa {
+
+namespace umma {
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (TMEM) (+)= A (shared memory descriptor) . B (shared memory descriptor)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D (TMEM) (+)= A (TMEM) . B (shared memory descriptor)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// One arrival on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane; the wait is in the same
+// statement so that no use of the values can be scheduled before it.
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared memory matrix descriptor: 128-byte swizzle, start address, leading and stride
+// byte offsets (16-byte units), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: f32 accumulator, A and B both bf16 (or both f16),
+// A K-major, B K-major or MN-major, M x N.
+__host__ __device__ constexpr uint32_t idesc(bool bf, bool b_mn_major, int M, int N) {
+  return (1u << 4) | ((bf ? 1u : 0u) << 7) | ((bf ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+}  // namespace umma
+
+constexpr uint32_t kUmmaWaitLimit = 1u << 20;  // mbarrier polls before a wait gives up
+constexpr float kUmmaSlack = 8.f;              // lazy running max, log2 units (p <= 256)
+constexpr float kUmmaEmpty = -1e30f;           // running max of a row with no visible token yet
+
+template <int KIND, int D>
+struct UmmaCfg {
+  static constexpr bool BF = KIND == KIND_BF16;
+  static constexpr int ROWS = 128, THREADS = 192;
+  static constexpr int NBOX = D / 64;                 // 64-element (128-byte) boxes per row
+  static constexpr int GP = 4;                        // pages per group: 64 tokens
+  static constexpr int R = D == 64 ? 16 : 8;          // page slots of the ring
+  static constexpr int NS = R / GP;                   // group slots
+  static constexpr int BOXB = kBlock * 128;           // one page's rows of one box: 2 KiB
+  static constexpr int QBOX = ROWS * 128;             // one box of the Q tile: 16 KiB
+  static constexpr int RING = R * BOXB;               // one box region of a ring
+  static constexpr int QOFF = 0, KOFF = NBOX * QBOX, VOFF = KOFF + NBOX * RING, BAR_OFF = VOFF + NBOX * RING;
+  static constexpr int NBARS = 2 * NS + 6;            // full, empty, s_full x2, p_full x2, o_done, drain
+  static constexpr size_t SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
+  static constexpr uint32_t TMEM_COLS = 256;          // S/P buffers at 0 and 64, O at 128
+  static constexpr uint32_t OCOL = 128;
+  static_assert(D % 64 == 0 && D <= 128, "head size 64 or 128");
+};
+
+// Bounded mbarrier wait that also gives up once another role has set *abort.
+__device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  for (uint32_t i = 0; i < kUmmaWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+template <int KIND, int D>
+__global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                                                            const __grid_constant__ CUtensorMap tmV) {
+  using C = UmmaCfg<KIND, D>;
+  using OutT = typename std::conditional<C::BF, __nv_bfloat16, __half>::type;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KiB alignment
+  uint8_t *sgen = smem_raw + (sbase - raw_u32);
+  const uint32_t qs = sbase + C::QOFF, ks = sbase + C::KOFF, vs = sbase + C::VOFF;
+  const uint32_t full0 = sbase + C::BAR_OFF, empty0 = full0 + 8 * C::NS, sfull0 = empty0 + 8 * C::NS;
+  const uint32_t pfull0 = sfull0 + 16, odone = pfull0 + 16, drain = odone + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + C::BAR_OFF + C::NBARS * 8);
+  volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *bad_block = reinterpret_cast<volatile int *>(tmem_slot + 2);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int G = p.G;
+
+  if (tid == 0) {
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sfull0 + 8 * b, 1);
+      mbar_init(pfull0 + 8 * b, 128);
+    }
+    mbar_init(odone, 1);
+    mbar_init(drain, 1);
+    *abort = 0;
+    *bad_block = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  grid_dependency_wait();
+
+  const int len = __ldg(p.seq_lens + s);
+  const int a = __ldg(p.qsl + s), b_end = __ldg(p.qsl + s + 1);
+  const int nq = b_end - a;
+  if (len < 0 || len > p.max_blocks * kBlock || a < 0 || b_end > p.Tq || nq < 0 || nq > p.nq_max || nq > len) {
+    if (tid == 0 && rt == 0 && g == 0 && p.err) atomicOr(p.err, kErrSeqLen);
+    return;
+  }
+  const int r0 = rt * C::ROWS;                  // first row of the CTA
+  const int nrows = min(C::ROWS, nq * G - r0);  // rows with a query token
+  if (nrows <= 0) return;
+  const int pos0 = len - nq;                    // row r sees tokens 0 .. pos0 + r / G
+  const int vis = pos0 + (r0 + nrows - 1) / G + 1;
+  const int npages = (vis + kBlock - 1) / kBlock;
+  const int ngr = (npages + C::GP - 1) / C::GP;
+
+  // ---- Q tile -> shared memory (128-byte swizzle, the layout TMA would give), zero rows past nrows
+  if (tid < C::ROWS) {
+    const int r = r0 + tid;
+    const bool valid = tid < nrows;
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        static_cast<const char *>(p.q) +
+        ((static_cast<int64_t>(a) + r / G) * p.q_ss + static_cast<int64_t>(g * G + r % G) * p.q_hs) * 2);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      const int box = c >> 3, ch = c & 7;
+      *reinterpret_cast<uint4 *>(sgen + C::QOFF + box * C::QBOX + (tid >> 3) * 1024 + (tid & 7) * 128 +
+                                 ((ch ^ (tid & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();  // generic writes -> the tensor core's async reads
+  }
+  if (warp == 4) {
+    umma::tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    umma::tmem_relinquish();
+  }
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+  // softmax state of row r0 + tid (threads 0-127), kept for the epilogue
+  const int row = r0 + tid;
+  const bool valid = tid < nrows;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // the warp's TMEM lanes
+  float l = 0.f;
+  bool ok = true;
+
+  if (warp == 5) {
+    // ------------------------------------------------------------ TMA producer
+    const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
+    const uint64_t pol = policy_evict_normal();  // the other row tiles of (s, g) read the same pages
+    const int c1 = p.nhd ? g : 0, c2 = p.nhd ? 0 : g;
+    int issued = 0;
+    for (int k = 0; k < ngr; ++k) {
+      const int gs = k % C::NS;
+      if (k >= C::NS && !__all_sync(0xffffffffu, umma_wait(empty0 + 8 * gs, ((k / C::NS) - 1) & 1, abort))) break;
+      const int npg = min(C::GP, npages - k * C::GP);
+      int pid = 0;
+      if (lane < npg) {
+        pid = __ldg(bt + k * C::GP + lane);
+        if (pid < 0 || pid >= p.num_blocks) {
+          *bad_block = 1;
+          if (p.err) atomicOr(p.err, kErrBlock);
+          pid = 0;  // load a valid block; the CTA writes nothing
+        }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * gs, npg * 2 * C::NBOX * C::BOXB);
+      __syncwarp();
+      if (lane < npg) {
+        const int slot = gs * C::GP + lane;
+#pragma unroll
+        for (int bx = 0; bx < C::NBOX; ++bx) {
+          tma_load_4d(ks + bx * C::RING + slot * C::BOXB, &tmK, full0 + 8 * gs, bx * 64, c1, c2, pid, pol);
+          tma_load_4d(vs + bx * C::RING + slot * C::BOXB, &tmV, full0 + 8 * gs, bx * 64, c1, c2, pid, pol);
+        }
+      }
+      issued = k + 1;
+    }
+    if (*abort && lane == 0) {
+      // loads may still be in flight into the ring: wait (bounded) for the latest group of
+      // every slot before the CTA's shared memory goes away
+      for (int k2 = max(0, issued - C::NS); k2 < issued; ++k2)
+        mbar_wait_bounded(full0 + 8 * (k2 % C::NS), (k2 / C::NS) & 1, kUmmaWaitLimit);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t iS = umma::idesc(C::BF, false, 128, 64);  // S = Q . K^T, N = 64 tokens
+      constexpr uint32_t iPV = umma::idesc(C::BF, true, 128, 64);  // O += P . V, N = 64 dims
+      for (int k = 0; k <= ngr; ++k) {
+        if (k < ngr) {
+          const int gs = k % C::NS;
+          if (!umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort)) break;
+          umma::fence_after();
+          const uint32_t d = tmem + 64u * (k & 1);
+          const uint32_t kgrp = ks + gs * C::GP * C::BOXB;
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            const uint32_t off = 32u * (j & 3);  // 16-element k step within the 128-byte row
+            const uint64_t ad = umma::sdesc(qs + (j >> 2) * C::QBOX + off, 16, 1024);
+            const uint64_t bd = umma::sdesc(kgrp + (j >> 2) * C::RING + off, 16, 1024);
+            umma::mma_ss(d, ad, bd, iS, j > 0 ? 1u : 0u);
+          }
+          umma::commit(sfull0 + 8 * (k & 1));
+        }
+        if (k >= 1) {
+          const int kp = k - 1, gsp = kp % C::NS, bp = kp & 1;
+          if (!umma_wait(pfull0 + 8 * bp, (kp >> 1) & 1, abort)) break;
+          umma::fence_after();
+          const int npg = min(C::GP, npages - kp * C::GP);
+          for (int i = 0; i < npg; ++i) {
+            const uint32_t phi = tmem + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
+#pragma unroll
+            for (int h = 0; h < C::NBOX; ++h) {
+              const uint64_t vd = umma::sdesc(vs + h * C::RING + (gsp * C::GP + i) * C::BOXB, 1024, 1024);
+              const uint32_t dO = tmem + C::OCOL + 64u * h;
+              umma::mma_ts(dO, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
+              umma::mma_ts(dO, phi + 8u, vd, iPV, 1u);
+            }
+          }
+          umma::commit(odone);
+          if (kp + C::NS < ngr) umma::commit(empty0 + 8 * gsp);  // only slots that are refilled
+        }
+      }
+      if (*abort) {
+        umma::commit(drain);  // every MMA issued so far has completed once this arrives
+        mbar_wait_bounded(drain, 0, kUmmaWaitLimit);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (row = tid)
+    const int pos = valid ? pos0 + row / G : -1;
+    const float ab = (p.alibi && valid) ? __ldg(p.alibi + g * G + row % G) * 1.4426950408889634f : 0.f;
+    float m = kUmmaEmpty;
+    for (int k = 0; k < ngr && ok; ++k) {
+      const int b = k & 1;
+      if (!__all_sync(0xffffffffu, umma_wait(sfull0 + 8 * b, (k >> 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
+      umma::fence_after();
+      float x[64];
+      {
+        float h0[32], h1[32];
+        umma::ld32(tl + 64u * b, h0);
+        umma::ld32(tl + 64u * b + 32u, h1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = h0[i];
+          x[32 + i] = h1[i];
+        }
+      }
+      const int t0 = k * C::GP * kBlock;
+      float lm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const int t = t0 + i;
+        x[i] = t <= pos ? fmaf(ab, static_cast<float>(t - pos), x[i] * p.scale_log2) : -INFINITY;
+        lm = fmaxf(lm, x[i]);
+      }
+      // P.V of the previous group has completed: O may be rescaled
+      if (k >= 1 && !__all_sync(0xffffffffu, umma_wait(odone, (k - 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
+      const bool need = lm > m + kUmmaSlack;
+      const float mn = need ? lm : m;
+      if (k >= 1 && __any_sync(0xffffffffu, need)) {
+        umma::fence_after();
+        const float al = ex2(m - mn);
+        l *= al;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          umma::ld32(tl + C::OCOL + 32u * c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= al;
+          umma::st32(tl + C::OCOL + 32u * c, o);
+        }
+        umma::wait_st();
+      }
+      m = mn;
+#pragma unroll
+      for (int pg = 0; pg < C::GP; ++pg) {
+        uint32_t w[16];  // 8 hi words, then 8 lo words, of the page's 16 tokens
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float u = ex2(x[16 * pg + 2 * i] - m), v = ex2(x[16 * pg + 2 * i + 1] - m);
+          l += u + v;
+          if constexpr (C::BF) {
+            w[i] = pack_bf16(u, v);
+            const float2 f = unpack_bf16(w[i]);
+            w[8 + i] = pack_bf16(u - f.x, v - f.y);
+          } else {
+            w[i] = pack_f16(u, v);
+            const float2 f = unpack_f16(w[i]);
+            w[8 + i] = pack_f16(u - f.x, v - f.y);
+          }
+        }
+        umma::st16(tl + 64u * b + 16u * pg, w);
+      }
+      umma::wait_st();
+      if (k == ngr - 1) {
+        // V rows of tokens >= len in the last page may hold anything (NaN included) and
+        // P . V would carry it into O even with P = 0 there: zero them
+        const int lastp = npages - 1, nv = min(kBlock, len - lastp * kBlock);
+        if (nv < kBlock) {
+          const int slot = (k % C::NS) * C::GP + (lastp - k * C::GP);
+          const int chunks = (kBlock - nv) * 8 * C::NBOX;  // 16-byte chunks
+          for (int c = tid; c < chunks; c += C::ROWS) {
+            const int bx = c / ((kBlock - nv) * 8), rr = (c / 8) % (kBlock - nv) + nv, ch = c % 8;
+            *reinterpret_cast<uint4 *>(sgen + C::VOFF + bx * C::RING + slot * C::BOXB + rr * 128 + ch * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+      }
+      umma::fence_before();
+      mbar_arrive(pfull0 + 8 * b);
+    }
+  }
+  // every role has left its loop (a block-table error it found is visible from here on)
+  umma::fence_before();
+  __syncthreads();
+  if (warp < 4) {
+    // ---- epilogue: O / l -> out
+    if (ok && __all_sync(0xffffffffu, umma_wait(odone, (ngr - 1) & 1, abort))) {
+      umma::fence_after();
+      const bool store = valid && !*bad_block;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      OutT *dst = static_cast<OutT *>(p.out) +
+                  (static_cast<int64_t>(a) + row / G) * p.out_ss + static_cast<int64_t>(g * G + row % G) * p.out_hs;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        umma::ld32(tl + C::OCOL + 32u * c, o);
+        if (store) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = C::BF ? pack_bf16(o[2 * i] * inv, o[2 * i + 1] * inv) : pack_f16(o[2 * i] * inv, o[2 * i + 1] * inv);
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+  }
+  umma::fence_before();
+  __syncthreads();
+  if (*abort && tid == 0 && p.err) atomicOr(p.err, kErrTimeout);
+  if (warp == 4) {
+    umma::fence_after();
+    umma::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int KIND, int D>
+struct UmmaLaunch {
+  using C = UmmaCfg<KIND, D>;
+  static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
+    auto kern = chunk_umma_kernel<KIND, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    const int rows = p.nq_max * p.G;
+    const dim3 grid((rows + C::ROWS - 1) / C::ROWS, p.Hkv, p.S);
+    e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, 1, p, tmK, tmV);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+};
+
+}  // namespace pa

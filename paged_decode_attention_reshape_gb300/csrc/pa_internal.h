@@ -127,12 +127,12 @@ cudaError_t launch_decode_mma_16(const DecodeParams &p, int kind, const CUtensor
 cudaError_t launch_decode_mma_fp8(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
                                   cudaStream_t st);  // KIND_FP8_*
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st);
-// Query-tile kernel for chunks of query tokens (pa_attention_varlen): bf16 / f16 caches,
-// head sizes 64 and 128; never splits the page range.
-cudaError_t launch_chunk_mma(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                             cudaStream_t st);
-// Query columns per KV head (max_query_len x G) from which varlen attention uses it: at 32
-// columns half of each 64-row tile is empty and the column-group kernels are faster.
+// Query-tile kernel for chunks of query tokens (pa_attention_varlen) on tcgen05 tensor
+// cores: bf16 / f16 caches, head sizes 64 and 128; never splits the page range.
+cudaError_t launch_chunk_umma(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                              cudaStream_t st);
+// Query columns per KV head (max_query_len x G) from which varlen attention uses it: below
+// 64 columns the column-group kernels are as fast or faster.
 constexpr int kChunkMinColumns = 64;
 // Resident CTAs per SM of a tensor-core instantiation (CUDA occupancy calculator:
 // shared memory, registers and threads); 0 when it cannot be queried.
