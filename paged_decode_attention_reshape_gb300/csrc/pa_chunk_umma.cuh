@@ -352,22 +352,42 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
           x[32 + i] = h1[i];
         }
       }
+      // ---- logits in log2 units, masked past the row's position; a group the whole warp
+      // sees in full (or rows without a query) skips the mask
       const int t0 = k * C::GP * kBlock;
-      float lm = -INFINITY;
+      const bool whole = __all_sync(0xffffffffu, t0 + 63 <= pos || !valid);
+      const float base = ab * static_cast<float>(t0 - pos);  // ALiBi bias of token t0
+      if (whole) {
+        if (p.alibi) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int t = t0 + i;
-        x[i] = t <= pos ? fmaf(ab, static_cast<float>(t - pos), x[i] * p.scale_log2) : -INFINITY;
-        lm = fmaxf(lm, x[i]);
+          for (int i = 0; i < 64; ++i) x[i] = fmaf(x[i], p.scale_log2, fmaf(ab, static_cast<float>(i), base));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) x[i] *= p.scale_log2;
+        }
+      } else {
+        const int lim = pos - t0;  // tokens i <= lim are visible
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          x[i] = i <= lim ? fmaf(x[i], p.scale_log2, fmaf(ab, static_cast<float>(i), base)) : -INFINITY;
       }
-      // P.V of the previous group has completed: O may be rescaled
-      if (k >= 1 && !__all_sync(0xffffffffu, umma_wait(odone, (k - 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
+      float mx[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(x[j], x[j + 8]), fmaxf(x[j + 16], x[j + 24]));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], fmaxf(fmaxf(x[j + 32], x[j + 40]), fmaxf(x[j + 48], x[j + 56])));
+      const float lm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool need = lm > m + kUmmaSlack;
       const float mn = need ? lm : m;
+      // P.V of the previous group must have completed before O is rescaled; every group
+      // waits for it once (below at the latest) so that the parity waits stay in step
+      bool waited = k == 0;
       if (k >= 1 && __any_sync(0xffffffffu, need)) {
+        if (!__all_sync(0xffffffffu, umma_wait(odone, (k - 1) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        waited = true;
         umma::fence_after();
         const float al = ex2(m - mn);
         l *= al;
@@ -382,13 +402,14 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
         umma::wait_st();
       }
       m = mn;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int pg = 0; pg < C::GP; ++pg) {
         uint32_t w[16];  // 8 hi words, then 8 lo words, of the page's 16 tokens
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float u = ex2(x[16 * pg + 2 * i] - m), v = ex2(x[16 * pg + 2 * i + 1] - m);
-          l += u + v;
+          ls[i] += u + v;
           if constexpr (C::BF) {
             w[i] = pack_bf16(u, v);
             const float2 f = unpack_bf16(w[i]);
@@ -401,7 +422,12 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
         }
         umma::st16(tl + 64u * b + 16u * pg, w);
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       umma::wait_st();
+      if (!waited && !__all_sync(0xffffffffu, umma_wait(odone, (k - 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
       if (k == ngr - 1) {
         // V rows of tokens >= len in the last page may hold anything (NaN included) and
         // P . V would carry it into O even with P = 0 there: zero them
