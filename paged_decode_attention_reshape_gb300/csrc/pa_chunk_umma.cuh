@@ -288,20 +288,23 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t iS = umma::idesc(C::BF, false, 128, 64);  // S = Q . K^T, N = 64 tokens
-      constexpr uint32_t iPV = umma::idesc(C::BF, true, 128, 64);  // O += P . V, N = 64 dims
+      constexpr uint32_t iPV = umma::idesc(C::BF, true, 128, D);   // O += P . V, N = D dims
+      // descriptors are built once; an operand at a byte offset adds offset / 16 to them
+      const uint64_t qd0 = umma::sdesc(qs, 16, 1024), kd0 = umma::sdesc(ks, 16, 1024);
+      // V (MN-major): 8-token row groups 1024 bytes apart, the 64-dim boxes one ring region apart
+      const uint64_t vd0 = umma::sdesc(vs, C::RING, 1024);
       for (int k = 0; k <= ngr; ++k) {
         if (k < ngr) {
           const int gs = k % C::NS;
           if (!umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort)) break;
           umma::fence_after();
           const uint32_t d = tmem + 64u * (k & 1);
-          const uint32_t kgrp = ks + gs * C::GP * C::BOXB;
+          const uint64_t kd = kd0 + ((gs * C::GP * C::BOXB) >> 4);
 #pragma unroll
           for (int j = 0; j < D / 16; ++j) {
-            const uint32_t off = 32u * (j & 3);  // 16-element k step within the 128-byte row
-            const uint64_t ad = umma::sdesc(qs + (j >> 2) * C::QBOX + off, 16, 1024);
-            const uint64_t bd = umma::sdesc(kgrp + (j >> 2) * C::RING + off, 16, 1024);
-            umma::mma_ss(d, ad, bd, iS, j > 0 ? 1u : 0u);
+            // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
+            umma::mma_ss(d, qd0 + (((j >> 2) * C::QBOX + 32 * (j & 3)) >> 4),
+                         kd + (((j >> 2) * C::RING + 32 * (j & 3)) >> 4), iS, j > 0 ? 1u : 0u);
           }
           umma::commit(sfull0 + 8 * (k & 1));
         }
@@ -312,13 +315,9 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
           const int npg = min(C::GP, npages - kp * C::GP);
           for (int i = 0; i < npg; ++i) {
             const uint32_t phi = tmem + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
-#pragma unroll
-            for (int h = 0; h < C::NBOX; ++h) {
-              const uint64_t vd = umma::sdesc(vs + h * C::RING + (gsp * C::GP + i) * C::BOXB, 1024, 1024);
-              const uint32_t dO = tmem + C::OCOL + 64u * h;
-              umma::mma_ts(dO, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
-              umma::mma_ts(dO, phi + 8u, vd, iPV, 1u);
-            }
+            const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
+            umma::mma_ts(tmem + C::OCOL, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
+            umma::mma_ts(tmem + C::OCOL, phi + 8u, vd, iPV, 1u);
           }
           umma::commit(odone);
           if (kp + C::NS < ngr) umma::commit(empty0 + 8 * gsp);  // only slots that are refilled
