@@ -41,6 +41,7 @@ from workloads import configs, data  # noqa: E402
 
 METRIC = "paged-decode KV-read GB/s (% of HBM peak), tokens/s; cache-write GB/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -58,6 +59,8 @@ class L2Flush:
         self.r.sum()
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma16.cu", "pa_decode_mma_fp8.cu", "pa_decode.cu",
                   "pa_device.cuh", "pa_internal.h", "pa_merge.cuh", "pa_api.cu"]
+# sources of the query-tile kernel (chunked prefill / long query chunks)
+CHUNK_SOURCES = ["pa_chunk_umma.cuh", "pa_chunk_mma16.cu", "pa_device.cuh", "pa_internal.h", "pa_api.cu"]
 
 
 # ----------------------------------------------------------------- staging
@@ -143,6 +146,9 @@ def workspace_for(st: Staged, partition_size: int):
     import paged_decode_attention_reshape_gb300 as pa
     w = st.w
     code = {"f32": pa.PA_F32, "bf16": pa.PA_BF16, "e4m3": pa.PA_FP8_E4M3}[w.cache_dtype]
+    if w.query_tile() and partition_size in (0, -1):
+        # the query-tile kernel runs unsplit and uses no workspace
+        return -1, 1, torch.zeros(16, dtype=torch.uint8, device=st.q.device)
     hq = w.Hq * w.nq   # varlen: query columns count as Hq * max_query_len heads
     P, nparts = pa.pa_decode_plan(w.S, hq, w.Hkv, w.D, w.max_blocks, code, 0, partition_size)
     nbytes = pa.pa_decode_workspace_size(w.S, hq, w.Hkv, w.D, w.max_blocks, P) \
@@ -178,32 +184,34 @@ def run_step(st: Staged, partition_size: int = 0, ws=None) -> None:
 
 # ------------------------------------------------------------ measurement
 
-def _peaks():
+def _peaks(key="hbm_gbs"):
+    """(peak, source): the measured HBM copy GB/s, or with key "bf16_tflops_sustained" the
+    measured cuBLAS bf16 TFLOP/s of a seconds-long loop."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return (FALLBACK_HBM_GBS if key == "hbm_gbs" else FALLBACK_BF16_TFLOPS_SUSTAINED), "fallback"
 
 
-def decode_source_hash() -> str:
+def decode_source_hash(sources=None) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_decode_attention_reshape_gb300", "csrc")
-    for name in DECODE_SOURCES:
+    for name in (sources or DECODE_SOURCES):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def _ncu_traffic(config: str):
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it was
-    taken at the current decode sources (else None)."""
+def _ncu_traffic(config: str, sources=None):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary, if it was
+    taken at the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = decode_source_hash()
+    cur = decode_source_hash(sources)
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -549,6 +557,20 @@ def main(argv=None):
     peak, peak_src = _peaks()
     achieved = dec_bytes / (dk_avg * 1e-3) / 1e9
     launches = wr_n + dk_n
+    if w.query_tile() and args.partition_size in (0, -1):
+        # tensor-bound: algorithmic FLOPs against the sustained bf16 peak (the kernel runs
+        # inside a seconds-long loop of steps)
+        flops = w.attention_flops()
+        tpeak, tsrc = _peaks("bf16_tflops_sustained")
+        tach = flops / (dk_avg * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": tach, "peak": tpeak, "unit": "TFLOP/s", "frac": tach / tpeak,
+                    "traffic": _ncu_traffic(w.name, CHUNK_SOURCES), "peak_source": tsrc + " (sustained)",
+                    "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": dec_bytes,
+                    "hbm_GB/s": achieved, "kernel": "chunk_umma_kernel"}
+    else:
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": _ncu_traffic(w.name), "peak_source": peak_src,
+                    "algorithmic_bytes_per_launch": dec_bytes, "kernel": "decode_mma_kernel"}
 
     e2e = None
     if not args.no_e2e:
@@ -573,9 +595,7 @@ def main(argv=None):
         "decode_kernel_us": dk_avg * 1e3,
         "cache_write": {"GB/s": w.write_bytes() / ((wr_ms / max(1, wr_n)) * 1e-3) / 1e9,
                         "kernel_us": wr_ms / max(1, wr_n) * 1e3, "bytes": w.write_bytes()},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": _ncu_traffic(w.name), "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": dec_bytes, "kernel": "decode_mma_kernel"},
+        "roofline": roofline,
         "gpu_launches": launches,
         "clocks": clocks,
         "e2e": e2e,

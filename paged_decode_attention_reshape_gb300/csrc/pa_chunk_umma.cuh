@@ -8,8 +8,8 @@
 // position len - n + i and sees the tokens up to it; the logit is scale q.k (+ the ALiBi
 // bias slope_h (t - position)).
 //
-// Work unit (one CTA): sequence s, KV head g and 128 query rows -- row r of the KV head
-// is query token r / G at head g G + r % G.  The page range is scanned in groups of 4
+// Work unit (one CTA): sequence s, KV head g and one or two tiles of 128 query rows --
+// row r of the KV head is query token r / G at head g G + r % G.  The page range is scanned in groups of 4
 // pages (64 tokens):
 //   S[128 x 64] = Q[128 x D] . K_group^T        tcgen05.mma, A and B from shared memory,
 //                                               S in tensor memory (TMEM)
@@ -18,9 +18,10 @@
 //                                               16-bit hi + lo halves (tcgen05.st)
 //   O[128 x D] += P[128 x 16] . V_page[16 x D]  tcgen05.mma per page and half, A = P from
 //                                               TMEM, B = the V page in shared memory
-// Roles (192 threads): warps 0-3 run the softmax and the epilogue (warp w owns TMEM lanes
-// and rows 32 w .. 32 w + 31), warp 4 allocates TMEM and its lane 0 issues the MMAs,
-// warp 5 resolves block_table and issues the TMA page loads into a ring of R page slots.
+// Roles (T tiles): warps 0 .. 4T-1 run the softmax and the epilogue (warp w belongs to
+// tile w / 4 and owns its TMEM lanes and rows 32 (w % 4) ..), warp 4T allocates TMEM and
+// its lane 0 issues the MMAs of every tile, warp 4T+1 resolves block_table and issues the
+// TMA page loads into a ring of R page slots.
 // Shared memory holds Q (loaded by the softmax threads, 128-byte swizzle) and the K and V
 // rings, one region per 64-element box of a row, so that the 16-token pages of a group
 // sit at one 1024-byte stride per 8 rows and form one MMA operand.  S and P of groups k
@@ -132,23 +133,31 @@ constexpr uint32_t kUmmaWaitLimit = 1u << 20;  // mbarrier polls before a wait g
 constexpr float kUmmaSlack = 8.f;              // lazy running max, log2 units (p <= 256)
 constexpr float kUmmaEmpty = -1e30f;           // running max of a row with no visible token yet
 
-template <int KIND, int D>
+// T row tiles of 128 rows per CTA.  T = 1: 6 warps, two CTAs per SM (their softmax and
+// MMA phases interleave).  T = 2: 10 warps, one CTA per SM; both tiles consume every K/V
+// page that is loaded once, and the ring is deeper.
+template <int KIND, int D, int T>
 struct UmmaCfg {
   static constexpr bool BF = KIND == KIND_BF16;
-  static constexpr int ROWS = 128, THREADS = 192;
+  static constexpr int TILES = T, ROWS = 128 * T;
+  static constexpr int MMA_WARP = 4 * T, TMA_WARP = 4 * T + 1, THREADS = (4 * T + 2) * 32;
+  static constexpr int MIN_CTAS = T == 1 ? 2 : 1;
   static constexpr int NBOX = D / 64;                 // 64-element (128-byte) boxes per row
   static constexpr int GP = 4;                        // pages per group: 64 tokens
-  static constexpr int R = D == 64 ? 16 : 8;          // page slots of the ring
+  static constexpr int R = T == 1 ? (D == 64 ? 16 : 8) : (D == 64 ? 40 : 20);  // page slots of the ring
   static constexpr int NS = R / GP;                   // group slots
   static constexpr int BOXB = kBlock * 128;           // one page's rows of one box: 2 KiB
-  static constexpr int QBOX = ROWS * 128;             // one box of the Q tile: 16 KiB
+  static constexpr int QBOX = 128 * 128;              // one box of one 128-row Q tile: 16 KiB
+  static constexpr int QTILE = NBOX * QBOX;           // one Q tile
   static constexpr int RING = R * BOXB;               // one box region of a ring
-  static constexpr int QOFF = 0, KOFF = NBOX * QBOX, VOFF = KOFF + NBOX * RING, BAR_OFF = VOFF + NBOX * RING;
-  static constexpr int NBARS = 2 * NS + 6;            // full, empty, s_full x2, p_full x2, o_done, drain
+  static constexpr int QOFF = 0, KOFF = T * QTILE, VOFF = KOFF + NBOX * RING, BAR_OFF = VOFF + NBOX * RING;
+  // barriers: full[NS], empty[NS]; per tile s_full x2, p_full x2, o_done (40 bytes); drain
+  static constexpr int TBAR = 2 * NS * 8, NBARS = 2 * NS + 5 * T + 1;
   static constexpr size_t SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
-  static constexpr uint32_t TMEM_COLS = 256;          // S/P buffers at 0 and 64, O at 128
+  static constexpr uint32_t TMEM_COLS = 256 * T;      // tile t: S/P buffers at 256 t + 0 / 64, O at 256 t + 128
   static constexpr uint32_t OCOL = 128;
   static_assert(D % 64 == 0 && D <= 128, "head size 64 or 128");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 // Bounded mbarrier wait that also gives up once another role has set *abort.
@@ -161,18 +170,23 @@ __device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, volatil
   return false;
 }
 
-template <int KIND, int D>
-__global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
-                                                            const __grid_constant__ CUtensorMap tmV) {
-  using C = UmmaCfg<KIND, D>;
+template <int KIND, int D, int T>
+__global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D, T>::MIN_CTAS)
+    chunk_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+  using C = UmmaCfg<KIND, D, T>;
   using OutT = typename std::conditional<C::BF, __nv_bfloat16, __half>::type;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KiB alignment
   uint8_t *sgen = smem_raw + (sbase - raw_u32);
   const uint32_t qs = sbase + C::QOFF, ks = sbase + C::KOFF, vs = sbase + C::VOFF;
-  const uint32_t full0 = sbase + C::BAR_OFF, empty0 = full0 + 8 * C::NS, sfull0 = empty0 + 8 * C::NS;
-  const uint32_t pfull0 = sfull0 + 16, odone = pfull0 + 16, drain = odone + 8;
+  const uint32_t full0 = sbase + C::BAR_OFF, empty0 = full0 + 8 * C::NS, tbar0 = full0 + C::TBAR;
+  // barriers of tile t
+  auto sfull = [&](int t, int b) { return tbar0 + 40u * t + 8u * b; };
+  auto pfull = [&](int t, int b) { return tbar0 + 40u * t + 16u + 8u * b; };
+  auto odone = [&](int t) { return tbar0 + 40u * t + 32u; };
+  const uint32_t drain = tbar0 + 40u * T;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + C::BAR_OFF + C::NBARS * 8);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *bad_block = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -186,11 +200,13 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(sfull0 + 8 * b, 1);
-      mbar_init(pfull0 + 8 * b, 128);
+    for (int t = 0; t < T; ++t) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(sfull(t, b), 1);
+        mbar_init(pfull(t, b), 128);
+      }
+      mbar_init(odone(t), 1);
     }
-    mbar_init(odone, 1);
     mbar_init(drain, 1);
     *abort = 0;
     *bad_block = 0;
@@ -210,14 +226,15 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
   const int r0 = rt * C::ROWS;                  // first row of the CTA
   const int nrows = min(C::ROWS, nq * G - r0);  // rows with a query token
   if (nrows <= 0) return;
+  const int ntiles = (nrows + 127) / 128;       // tiles with a query row
   const int pos0 = len - nq;                    // row r sees tokens 0 .. pos0 + r / G
   const int vis = pos0 + (r0 + nrows - 1) / G + 1;
   const int npages = (vis + kBlock - 1) / kBlock;
   const int ngr = (npages + C::GP - 1) / C::GP;
 
-  // ---- Q tile -> shared memory (128-byte swizzle, the layout TMA would give), zero rows past nrows
+  // ---- Q tiles -> shared memory (128-byte swizzle, the layout TMA would give), zero rows past nrows
   if (tid < C::ROWS) {
-    const int r = r0 + tid;
+    const int r = r0 + tid, tr = tid & 127;
     const bool valid = tid < nrows;
     const uint4 *src = reinterpret_cast<const uint4 *>(
         static_cast<const char *>(p.q) +
@@ -226,12 +243,12 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
     for (int c = 0; c < D / 8; ++c) {
       const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
       const int box = c >> 3, ch = c & 7;
-      *reinterpret_cast<uint4 *>(sgen + C::QOFF + box * C::QBOX + (tid >> 3) * 1024 + (tid & 7) * 128 +
-                                 ((ch ^ (tid & 7)) << 4)) = v;
+      *reinterpret_cast<uint4 *>(sgen + C::QOFF + (tid >> 7) * C::QTILE + box * C::QBOX + (tr >> 3) * 1024 +
+                                 (tr & 7) * 128 + ((ch ^ (tr & 7)) << 4)) = v;
     }
     fence_proxy_async_smem();  // generic writes -> the tensor core's async reads
   }
-  if (warp == 4) {
+  if (warp == C::MMA_WARP) {
     umma::tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     umma::tmem_relinquish();
   }
@@ -240,14 +257,16 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
   umma::fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
 
-  // softmax state of row r0 + tid (threads 0-127), kept for the epilogue
+  // softmax state of row r0 + tid (threads below ROWS: tile tid / 128), kept for the epilogue
   const int row = r0 + tid;
   const bool valid = tid < nrows;
-  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // the warp's TMEM lanes
+  const int tile = warp >> 2;
+  // the warp's TMEM lanes (a warp reaches lanes 32 (warp % 4) ..) in its tile's columns
+  const uint32_t tl = tmem + 256u * tile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
   float l = 0.f;
   bool ok = true;
 
-  if (warp == 5) {
+  if (warp == C::TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
     const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
     const uint64_t pol = policy_evict_normal();  // the other row tiles of (s, g) read the same pages
@@ -284,7 +303,7 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
       for (int k2 = max(0, issued - C::NS); k2 < issued; ++k2)
         mbar_wait_bounded(full0 + 8 * (k2 % C::NS), (k2 / C::NS) & 1, kUmmaWaitLimit);
     }
-  } else if (warp == 4) {
+  } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t iS = umma::idesc(C::BF, false, 128, 64);  // S = Q . K^T, N = 64 tokens
@@ -293,34 +312,43 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
       const uint64_t qd0 = umma::sdesc(qs, 16, 1024), kd0 = umma::sdesc(ks, 16, 1024);
       // V (MN-major): 8-token row groups 1024 bytes apart, the 64-dim boxes one ring region apart
       const uint64_t vd0 = umma::sdesc(vs, C::RING, 1024);
-      for (int k = 0; k <= ngr; ++k) {
+      bool stop = false;
+      for (int k = 0; k <= ngr && !stop; ++k) {
         if (k < ngr) {
           const int gs = k % C::NS;
           if (!umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort)) break;
           umma::fence_after();
-          const uint32_t d = tmem + 64u * (k & 1);
           const uint64_t kd = kd0 + ((gs * C::GP * C::BOXB) >> 4);
+          for (int t = 0; t < ntiles; ++t) {
+            const uint32_t d = tmem + 256u * t + 64u * (k & 1);
+            const uint64_t qd = qd0 + ((t * C::QTILE) >> 4);
 #pragma unroll
-          for (int j = 0; j < D / 16; ++j) {
-            // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
-            umma::mma_ss(d, qd0 + (((j >> 2) * C::QBOX + 32 * (j & 3)) >> 4),
-                         kd + (((j >> 2) * C::RING + 32 * (j & 3)) >> 4), iS, j > 0 ? 1u : 0u);
+            for (int j = 0; j < D / 16; ++j) {
+              // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
+              umma::mma_ss(d, qd + (((j >> 2) * C::QBOX + 32 * (j & 3)) >> 4),
+                           kd + (((j >> 2) * C::RING + 32 * (j & 3)) >> 4), iS, j > 0 ? 1u : 0u);
+            }
+            umma::commit(sfull(t, k & 1));
           }
-          umma::commit(sfull0 + 8 * (k & 1));
         }
         if (k >= 1) {
           const int kp = k - 1, gsp = kp % C::NS, bp = kp & 1;
-          if (!umma_wait(pfull0 + 8 * bp, (kp >> 1) & 1, abort)) break;
-          umma::fence_after();
           const int npg = min(C::GP, npages - kp * C::GP);
-          for (int i = 0; i < npg; ++i) {
-            const uint32_t phi = tmem + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
-            const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
-            umma::mma_ts(tmem + C::OCOL, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
-            umma::mma_ts(tmem + C::OCOL, phi + 8u, vd, iPV, 1u);
+          for (int t = 0; t < ntiles; ++t) {
+            if (!umma_wait(pfull(t, bp), (kp >> 1) & 1, abort)) {
+              stop = true;
+              break;
+            }
+            umma::fence_after();
+            for (int i = 0; i < npg; ++i) {
+              const uint32_t phi = tmem + 256u * t + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
+              const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
+              umma::mma_ts(tmem + 256u * t + C::OCOL, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
+              umma::mma_ts(tmem + 256u * t + C::OCOL, phi + 8u, vd, iPV, 1u);
+            }
+            umma::commit(odone(t));
           }
-          umma::commit(odone);
-          if (kp + C::NS < ngr) umma::commit(empty0 + 8 * gsp);  // only slots that are refilled
+          if (!stop && kp + C::NS < ngr) umma::commit(empty0 + 8 * gsp);  // only slots that are refilled
         }
       }
       if (*abort) {
@@ -328,14 +356,14 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
         mbar_wait_bounded(drain, 0, kUmmaWaitLimit);
       }
     }
-  } else {
+  } else if (tile < ntiles) {
     // ------------------------------------------------------------ softmax (row = tid)
     const int pos = valid ? pos0 + row / G : -1;
     const float ab = (p.alibi && valid) ? __ldg(p.alibi + g * G + row % G) * 1.4426950408889634f : 0.f;
     float m = kUmmaEmpty;
     for (int k = 0; k < ngr && ok; ++k) {
       const int b = k & 1;
-      if (!__all_sync(0xffffffffu, umma_wait(sfull0 + 8 * b, (k >> 1) & 1, abort))) {
+      if (!__all_sync(0xffffffffu, umma_wait(sfull(tile, b), (k >> 1) & 1, abort))) {
         ok = false;
         break;
       }
@@ -382,7 +410,7 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
       // waits for it once (below at the latest) so that the parity waits stay in step
       bool waited = k == 0;
       if (k >= 1 && __any_sync(0xffffffffu, need)) {
-        if (!__all_sync(0xffffffffu, umma_wait(odone, (k - 1) & 1, abort))) {
+        if (!__all_sync(0xffffffffu, umma_wait(odone(tile), (k - 1) & 1, abort))) {
           ok = false;
           break;
         }
@@ -423,18 +451,19 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       umma::wait_st();
-      if (!waited && !__all_sync(0xffffffffu, umma_wait(odone, (k - 1) & 1, abort))) {
+      if (!waited && !__all_sync(0xffffffffu, umma_wait(odone(tile), (k - 1) & 1, abort))) {
         ok = false;
         break;
       }
-      if (k == ngr - 1) {
+      if (k == ngr - 1 && tile == 0) {
         // V rows of tokens >= len in the last page may hold anything (NaN included) and
-        // P . V would carry it into O even with P = 0 there: zero them
+        // P . V would carry it into O even with P = 0 there: tile 0 zeroes them before it
+        // hands over its P (the P . V of every tile is issued after that)
         const int lastp = npages - 1, nv = min(kBlock, len - lastp * kBlock);
         if (nv < kBlock) {
           const int slot = (k % C::NS) * C::GP + (lastp - k * C::GP);
           const int chunks = (kBlock - nv) * 8 * C::NBOX;  // 16-byte chunks
-          for (int c = tid; c < chunks; c += C::ROWS) {
+          for (int c = tid; c < chunks; c += 128) {
             const int bx = c / ((kBlock - nv) * 8), rr = (c / 8) % (kBlock - nv) + nv, ch = c % 8;
             *reinterpret_cast<uint4 *>(sgen + C::VOFF + bx * C::RING + slot * C::BOXB + rr * 128 + ch * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
@@ -443,15 +472,15 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
         }
       }
       umma::fence_before();
-      mbar_arrive(pfull0 + 8 * b);
+      mbar_arrive(pfull(tile, b));
     }
   }
   // every role has left its loop (a block-table error it found is visible from here on)
   umma::fence_before();
   __syncthreads();
-  if (warp < 4) {
+  if (warp < 4 * T && tile < ntiles) {
     // ---- epilogue: O / l -> out
-    if (ok && __all_sync(0xffffffffu, umma_wait(odone, (ngr - 1) & 1, abort))) {
+    if (ok && __all_sync(0xffffffffu, umma_wait(odone(tile), (ngr - 1) & 1, abort))) {
       umma::fence_after();
       const bool store = valid && !*bad_block;
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -476,17 +505,17 @@ __global__ void __launch_bounds__(192, 2) chunk_umma_kernel(const DecodeParams p
   umma::fence_before();
   __syncthreads();
   if (*abort && tid == 0 && p.err) atomicOr(p.err, kErrTimeout);
-  if (warp == 4) {
+  if (warp == C::MMA_WARP) {
     umma::fence_after();
     umma::tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-template <int KIND, int D>
+template <int KIND, int D, int T>
 struct UmmaLaunch {
-  using C = UmmaCfg<KIND, D>;
+  using C = UmmaCfg<KIND, D, T>;
   static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
-    auto kern = chunk_umma_kernel<KIND, D>;
+    auto kern = chunk_umma_kernel<KIND, D, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);

@@ -134,6 +134,9 @@ cudaError_t launch_chunk_umma(const DecodeParams &p, int kind, const CUtensorMap
 // Query columns per KV head (max_query_len x G) from which varlen attention uses it: below
 // 64 columns the column-group kernels are as fast or faster.
 constexpr int kChunkMinColumns = 64;
+// Query columns per KV head above which the query-tile kernel takes two 128-row tiles per
+// CTA (head size 128).
+constexpr int kChunkTwoTileColumns = 128;
 // Resident CTAs per SM of a tensor-core instantiation (CUDA occupancy calculator:
 // shared memory, registers and threads); 0 when it cannot be queried.
 int occupancy_decode_mma_16(int kind, int D);

@@ -239,3 +239,22 @@ def test_c3_spec4_write_and_sampled_varlen():
         ref = oracle_rows(w, int(s), heads)
         assert_close(got[s * w.nq:(s + 1) * w.nq][:, heads], ref, "c3-spec4 seq %d" % s)
     assert_close(got, step(st, -1), "plan vs unsplit")
+
+
+def test_c3_chunk128_write_and_sampled_query_tile():
+    """Chunked prefill at full size (256 sequences x 128 new tokens, 512 query rows per KV
+    head, the query-tile tensor-core kernel): the step's write, sampled sequences and heads
+    against the oracle, and the column-group path (fixed 4096-token partitions) on the same
+    step to the same bar."""
+    w = configs.get("c3-chunk128")
+    assert w.query_tile()
+    st = bench.stage(w)
+    got = step(st, 0)
+    rng = np.random.default_rng(128)
+    nvalid = int((w.step_slot >= 0).sum())
+    check_step_write(st, rows=np.sort(rng.choice(nvalid, size=512, replace=False)))
+    for s in rng.choice(w.S, size=4, replace=False):
+        heads = sorted(rng.choice(w.Hq, size=3, replace=False).tolist())
+        ref = oracle_rows(w, int(s), heads)
+        assert_close(got[s * w.nq:(s + 1) * w.nq][:, heads], ref, "c3-chunk128 seq %d" % s)
+    assert_close(got, step(st, 4096), "query tile vs column groups")

@@ -33,7 +33,8 @@ c5  write: 8192 rows = the last 64 positions of 128 sequences, 5% of them
 
 Variants with the same values: c2-nhd (NHD cache layout), c3-alibi (ALiBi
 slopes), c5-heads (one FP8 scale per KV head), c3-spec4 (4 query tokens per
-sequence, varlen attention; the first token's q is c3's).
+sequence, varlen attention; the first token's q is c3's), c3-chunk128 (128 new tokens
+per sequence: a chunked-prefill step).
 """
 from __future__ import annotations
 
@@ -120,6 +121,20 @@ class Workload:
         qo = 2 * self.S * self.nq * self.Hq * self.D * self.in_elem_bytes()
         qsl = (self.S + 1) * 4 if self.nq > 1 else 0
         return kv + qo + nb * 4 + self.S * 4 + qsl
+
+    def attention_flops(self) -> float:
+        """Algorithmic FLOPs of one attention call: q.k and p.v, 2 D each, for every (query
+        head, visible key) pair; new token i of n sits at position L - n + i and sees i + 1
+        + (L - n) keys."""
+        n = self.nq
+        pairs = sum(n * int(L) - n * (n - 1) // 2 for L in self.seq_lens)
+        return 4.0 * self.D * self.Hq * pairs
+
+    def query_tile(self) -> bool:
+        """True when attention runs on the query-tile tensor-core kernel: 64 or more query
+        columns (new tokens x G) per KV head, a 16-bit cache, head size 64 or 128."""
+        return (self.nq > 1 and self.nq * self.G >= 64 and self.cache_dtype in ("bf16", "f16")
+                and self.D in (64, 128))
 
     def write_bytes(self) -> int:
         """Algorithmic bytes of one cache write: valid rows read and written, plus slot_mapping."""
@@ -263,8 +278,19 @@ def c5_heads() -> Workload:
 def c3_spec4() -> Workload:
     """c3 with 4 new query tokens per sequence (speculative decoding: one token plus three
     draft tokens): the step writes each sequence's last 4 positions and attends causally."""
+    return _c3_new_tokens("c3-spec4", 4)
+
+
+def c3_chunk128() -> Workload:
+    """c3 as one chunked-prefill step: the last 128 positions of each of the 256 sequences are
+    new (32768 rows written), every new token attends causally to its history and the chunk
+    -- 512 query rows per KV head, the query-tile tensor-core kernel's case."""
+    return _c3_new_tokens("c3-chunk128", 128)
+
+
+def _c3_new_tokens(name: str, nq: int) -> Workload:
     w = c3()
-    w.name, w.nq = "c3-spec4", 4
+    w.name, w.nq = name, nq
     seqs = np.repeat(np.arange(w.S, dtype=np.int64), w.nq)
     pos = np.concatenate([np.arange(int(L) - w.nq, int(L), dtype=np.int64) for L in w.seq_lens])
     w.step_seq, w.step_pos = seqs, pos
@@ -273,7 +299,7 @@ def c3_spec4() -> Workload:
 
 
 BUILDERS = {"c1": c1, "c2": c2, "c3": c3, "c4": c4, "c5": c5, "c2-nhd": c2_nhd, "c3-alibi": c3_alibi,
-            "c5-heads": c5_heads, "c3-spec4": c3_spec4}
+            "c5-heads": c5_heads, "c3-spec4": c3_spec4, "c3-chunk128": c3_chunk128}
 
 
 def get(name: str) -> Workload:
