@@ -114,6 +114,15 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(r)::"memory");
+  return r != 0;
+}
+
 // Shared memory matrix descriptor: 128-byte swizzle, start address, leading and stride
 // byte offsets (16-byte units), descriptor version 1.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -305,7 +314,9 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop, so descriptors and addresses are warp-uniform values;
+    // one elected lane issues each batch of MMAs and its commit.
+    {
       constexpr uint32_t iS = umma::idesc(C::BF, false, 128, 64);  // S = Q . K^T, N = 64 tokens
       constexpr uint32_t iPV = umma::idesc(C::BF, true, 128, D);   // O += P . V, N = D dims
       // descriptors are built once; an operand at a byte offset adds offset / 16 to them
@@ -316,43 +327,54 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       for (int k = 0; k <= ngr && !stop; ++k) {
         if (k < ngr) {
           const int gs = k % C::NS;
-          if (!umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort)) break;
+          if (!__all_sync(0xffffffffu, umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort))) break;
           umma::fence_after();
           const uint64_t kd = kd0 + ((gs * C::GP * C::BOXB) >> 4);
           for (int t = 0; t < ntiles; ++t) {
             const uint32_t d = tmem + 256u * t + 64u * (k & 1);
             const uint64_t qd = qd0 + ((t * C::QTILE) >> 4);
+            if (umma::elect_one()) {
 #pragma unroll
-            for (int j = 0; j < D / 16; ++j) {
-              // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
-              umma::mma_ss(d, qd + (((j >> 2) * C::QBOX + 32 * (j & 3)) >> 4),
-                           kd + (((j >> 2) * C::RING + 32 * (j & 3)) >> 4), iS, j > 0 ? 1u : 0u);
+              for (int j = 0; j < D / 16; ++j) {
+                // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
+                umma::mma_ss(d, qd + (((j >> 2) * C::QBOX + 32 * (j & 3)) >> 4),
+                             kd + (((j >> 2) * C::RING + 32 * (j & 3)) >> 4), iS, j > 0 ? 1u : 0u);
+              }
+              umma::commit(sfull(t, k & 1));
             }
-            umma::commit(sfull(t, k & 1));
+            __syncwarp();
           }
         }
         if (k >= 1) {
           const int kp = k - 1, gsp = kp % C::NS, bp = kp & 1;
           const int npg = min(C::GP, npages - kp * C::GP);
           for (int t = 0; t < ntiles; ++t) {
-            if (!umma_wait(pfull(t, bp), (kp >> 1) & 1, abort)) {
+            if (!__all_sync(0xffffffffu, umma_wait(pfull(t, bp), (kp >> 1) & 1, abort))) {
               stop = true;
               break;
             }
             umma::fence_after();
-            for (int i = 0; i < npg; ++i) {
-              const uint32_t phi = tmem + 256u * t + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
-              const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
-              umma::mma_ts(tmem + 256u * t + C::OCOL, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
-              umma::mma_ts(tmem + 256u * t + C::OCOL, phi + 8u, vd, iPV, 1u);
+            const uint32_t dO = tmem + 256u * t + C::OCOL;
+            if (umma::elect_one()) {
+              for (int i = 0; i < npg; ++i) {
+                const uint32_t phi = tmem + 256u * t + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
+                const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
+                umma::mma_ts(dO, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
+                umma::mma_ts(dO, phi + 8u, vd, iPV, 1u);
+              }
+              umma::commit(odone(t));
             }
-            umma::commit(odone(t));
+            __syncwarp();
           }
-          if (!stop && kp + C::NS < ngr) umma::commit(empty0 + 8 * gsp);  // only slots that are refilled
+          if (!stop && kp + C::NS < ngr) {  // only slots that are refilled
+            if (umma::elect_one()) umma::commit(empty0 + 8 * gsp);
+            __syncwarp();
+          }
         }
       }
       if (*abort) {
-        umma::commit(drain);  // every MMA issued so far has completed once this arrives
+        if (umma::elect_one()) umma::commit(drain);  // every MMA issued so far has completed once this arrives
+        __syncwarp();
         mbar_wait_bounded(drain, 0, kUmmaWaitLimit);
       }
     }
