@@ -174,7 +174,8 @@ template <int KIND, int D, int T>
 struct UmmaCfg {
   static constexpr bool BF = KIND == KIND_BF16;
   static constexpr int TILES = T, ROWS = 128 * T;
-  static constexpr int MMA_WARP = 4 * T, TMA_WARP = 4 * T + 1, THREADS = (4 * T + 2) * 32;
+  // warps 0 .. 4T-1 softmax, 4T .. 5T-1 one MMA issuer per tile, 5T the TMA producer
+  static constexpr int MMA_WARP = 4 * T, TMA_WARP = 5 * T, THREADS = (5 * T + 1) * 32;
   static constexpr int MIN_CTAS = T == 1 ? 2 : 1;
   static constexpr int NBOX = D / 64;                 // 64-element (128-byte) boxes per row
   static constexpr int GP = 4;                        // pages per group: 64 tokens
@@ -185,8 +186,8 @@ struct UmmaCfg {
   static constexpr int QTILE = NBOX * QBOX;           // one Q tile
   static constexpr int RING = R * BOXB;               // one box region of a ring
   static constexpr int QOFF = 0, KOFF = T * QTILE, VOFF = KOFF + NBOX * RING, BAR_OFF = VOFF + NBOX * RING;
-  // barriers: full[NS], empty[NS]; per tile s_full x2, p_full x2, o_done (40 bytes); drain
-  static constexpr int TBAR = 2 * NS * 8, NBARS = 2 * NS + 5 * T + 1;
+  // barriers: full[NS], empty[NS]; per tile s_full x2, p_full x2, o_done, drain (48 bytes)
+  static constexpr int TBAR = 2 * NS * 8, NBARS = 2 * NS + 6 * T;
   static constexpr size_t SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 256 * T;      // tile t: S/P buffers at 256 t + 0 / 64, O at 256 t + 128
   static constexpr uint32_t OCOL = 128;
@@ -217,10 +218,10 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   const uint32_t qs = sbase + C::QOFF, ks = sbase + C::KOFF, vs = sbase + C::VOFF;
   const uint32_t full0 = sbase + C::BAR_OFF, empty0 = full0 + 8 * C::NS, tbar0 = full0 + C::TBAR;
   // barriers of tile t
-  auto sfull = [&](int t, int b) { return tbar0 + 40u * t + 8u * b; };
-  auto pfull = [&](int t, int b) { return tbar0 + 40u * t + 16u + 8u * b; };
-  auto odone = [&](int t) { return tbar0 + 40u * t + 32u; };
-  const uint32_t drain = tbar0 + 40u * T;
+  auto sfull = [&](int t, int b) { return tbar0 + 48u * t + 8u * b; };
+  auto pfull = [&](int t, int b) { return tbar0 + 48u * t + 16u + 8u * b; };
+  auto odone = [&](int t) { return tbar0 + 48u * t + 32u; };
+  auto drain = [&](int t) { return tbar0 + 48u * t + 40u; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + C::BAR_OFF + C::NBARS * 8);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *bad_block = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -230,21 +231,6 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   const int G = p.G;
 
   if (tid == 0) {
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 1);
-    }
-    for (int t = 0; t < T; ++t) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(sfull(t, b), 1);
-        mbar_init(pfull(t, b), 128);
-      }
-      mbar_init(odone(t), 1);
-    }
-    mbar_init(drain, 1);
-    *abort = 0;
-    *bad_block = 0;
-    fence_barrier_init();
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
@@ -265,6 +251,23 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   const int vis = pos0 + (r0 + nrows - 1) / G + 1;
   const int npages = (vis + kBlock - 1) / kBlock;
   const int ngr = (npages + C::GP - 1) / C::GP;
+  if (tid == 0) {
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, ntiles);  // one commit per active tile's issuer
+    }
+    for (int t = 0; t < T; ++t) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(sfull(t, b), 1);
+        mbar_init(pfull(t, b), 128);
+      }
+      mbar_init(odone(t), 1);
+      mbar_init(drain(t), 1);
+    }
+    *abort = 0;
+    *bad_block = 0;
+    fence_barrier_init();
+  }
 
   // ---- Q tiles -> shared memory (128-byte swizzle, the layout TMA would give), zero rows past nrows
   if (tid < C::ROWS) {
@@ -337,70 +340,65 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       for (int k2 = max(0, issued - C::NS); k2 < issued; ++k2)
         mbar_wait_bounded(full0 + 8 * (k2 % C::NS), (k2 / C::NS) & 1, kUmmaWaitLimit);
     }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer of tile t
     // The whole warp runs the loop, so descriptors and addresses are warp-uniform values;
-    // one elected lane issues each batch of MMAs and its commit.
-    {
+    // one elected lane issues each batch of MMAs and its commit.  Each tile has its own
+    // issuer, so a tile whose softmax runs late does not hold back the other.
+    const int t = warp - C::MMA_WARP;
+    if (t < ntiles) {
       constexpr uint32_t iS = umma::idesc(C::BF, false, 128, 64);  // S = Q . K^T, N = 64 tokens
       constexpr uint32_t iPV = umma::idesc(C::BF, true, 128, D);   // O += P . V, N = D dims
       // descriptors are built once; an operand at a byte offset adds offset / 16 to them
-      const uint64_t qd0 = umma::sdesc(qs, 16, 1024), kd0 = umma::sdesc(ks, 16, 1024);
+      const uint64_t qd = umma::sdesc(qs + t * C::QTILE, 16, 1024), kd0 = umma::sdesc(ks, 16, 1024);
       // V (MN-major): 8-token row groups 1024 bytes apart, the 64-dim boxes one ring region apart
       const uint64_t vd0 = umma::sdesc(vs, C::RING, 1024);
-      bool stop = false;
-      for (int k = 0; k <= ngr && !stop; ++k) {
+      const uint32_t tt = tmem + 256u * t;  // the tile's TMEM columns
+      const bool vtail = len - (npages - 1) * kBlock < kBlock;  // the last page has rows past len
+      for (int k = 0; k <= ngr; ++k) {
         if (k < ngr) {
           const int gs = k % C::NS;
           if (!__all_sync(0xffffffffu, umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort))) break;
           umma::fence_after();
           const uint64_t kd = kd0 + ((gs * C::GP * C::BOXB) >> 4);
-          for (int t = 0; t < ntiles; ++t) {
-            const uint32_t d = tmem + 256u * t + 64u * (k & 1);
-            const uint64_t qd = qd0 + ((t * C::QTILE) >> 4);
-            if (umma::elect_one()) {
+          if (umma::elect_one()) {
 #pragma unroll
-              for (int j = 0; j < D / 16; ++j) {
-                // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
-                umma::mma_ss(d, qd + (((j >> 2) * C::QBOX + 32 * (j & 3)) >> 4),
-                             kd + (((j >> 2) * C::RING + 32 * (j & 3)) >> 4), iS, j > 0 ? 1u : 0u);
-              }
-              umma::commit(sfull(t, k & 1));
+            for (int j = 0; j < D / 16; ++j) {
+              // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
+              umma::mma_ss(tt + 64u * (k & 1), qd + (((j >> 2) * C::QBOX + 32 * (j & 3)) >> 4),
+                           kd + (((j >> 2) * C::RING + 32 * (j & 3)) >> 4), iS, j > 0 ? 1u : 0u);
             }
-            __syncwarp();
+            umma::commit(sfull(t, k & 1));
           }
+          __syncwarp();
         }
         if (k >= 1) {
           const int kp = k - 1, gsp = kp % C::NS, bp = kp & 1;
           const int npg = min(C::GP, npages - kp * C::GP);
-          for (int t = 0; t < ntiles; ++t) {
-            if (!__all_sync(0xffffffffu, umma_wait(pfull(t, bp), (kp >> 1) & 1, abort))) {
-              stop = true;
-              break;
+          if (!__all_sync(0xffffffffu, umma_wait(pfull(t, bp), (kp >> 1) & 1, abort))) break;
+          // the last page's V tail is zeroed by tile 0 before it hands over its P: the other
+          // tiles' last P.V waits for that too (the final phase of tile 0's barrier)
+          if (t > 0 && kp == ngr - 1 && vtail &&
+              !__all_sync(0xffffffffu, umma_wait(pfull(0, bp), (kp >> 1) & 1, abort)))
+            break;
+          umma::fence_after();
+          if (umma::elect_one()) {
+            for (int i = 0; i < npg; ++i) {
+              const uint32_t phi = tt + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
+              const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
+              umma::mma_ts(tt + C::OCOL, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
+              umma::mma_ts(tt + C::OCOL, phi + 8u, vd, iPV, 1u);
             }
-            umma::fence_after();
-            const uint32_t dO = tmem + 256u * t + C::OCOL;
-            if (umma::elect_one()) {
-              for (int i = 0; i < npg; ++i) {
-                const uint32_t phi = tmem + 256u * t + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
-                const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
-                umma::mma_ts(dO, phi, vd, iPV, (kp > 0 || i > 0) ? 1u : 0u);
-                umma::mma_ts(dO, phi + 8u, vd, iPV, 1u);
-              }
-              umma::commit(odone(t));
-            }
-            __syncwarp();
+            umma::commit(odone(t));
+            if (kp + C::NS < ngr) umma::commit(empty0 + 8 * gsp);  // only slots that are refilled
           }
-          if (!stop && kp + C::NS < ngr) {  // only slots that are refilled
-            if (umma::elect_one()) umma::commit(empty0 + 8 * gsp);
-            __syncwarp();
-          }
+          __syncwarp();
         }
       }
       if (*abort) {
-        if (umma::elect_one()) umma::commit(drain);  // every MMA issued so far has completed once this arrives
+        if (umma::elect_one()) umma::commit(drain(t));  // every MMA of this issuer has completed once this arrives
         __syncwarp();
-        mbar_wait_bounded(drain, 0, kUmmaWaitLimit);
+        mbar_wait_bounded(drain(t), 0, kUmmaWaitLimit);
       }
     }
   } else if (tile < ntiles) {
