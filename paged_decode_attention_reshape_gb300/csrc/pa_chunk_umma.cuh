@@ -428,13 +428,13 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       const int t0 = k * C::GP * kBlock;
       const bool whole = __all_sync(0xffffffffu, t0 + 63 <= pos || !valid);
       const float base = ab * static_cast<float>(t0 - pos);  // ALiBi bias of token t0
+      // raw: the scores stay unscaled (scale > 0 keeps their order) and the scale is folded
+      // into the exponent below; otherwise x holds the biased / masked log2 logits
+      const bool raw = whole && !p.alibi;
       if (whole) {
         if (p.alibi) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) x[i] = fmaf(x[i], p.scale_log2, fmaf(ab, static_cast<float>(i), base));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] *= p.scale_log2;
         }
       } else {
         const int lim = pos - t0;  // tokens i <= lim are visible
@@ -447,7 +447,9 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(x[j], x[j + 8]), fmaxf(x[j + 16], x[j + 24]));
 #pragma unroll
       for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], fmaxf(fmaxf(x[j + 32], x[j + 40]), fmaxf(x[j + 48], x[j + 56])));
-      const float lm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float lm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                       (raw ? p.scale_log2 : 1.f);
+      const float sc = raw ? p.scale_log2 : 1.f;  // p = exp2(x sc - m)
       const bool need = lm > m + kUmmaSlack;
       const float mn = need ? lm : m;
       // P.V of the previous group must have completed before O is rescaled; every group
@@ -479,7 +481,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
         uint32_t w[16];  // 8 hi words, then 8 lo words, of the page's 16 tokens
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float u = ex2(x[16 * pg + 2 * i] - m), v = ex2(x[16 * pg + 2 * i + 1] - m);
+          const float u = ex2(fmaf(x[16 * pg + 2 * i], sc, -m)), v = ex2(fmaf(x[16 * pg + 2 * i + 1], sc, -m));
           ls[i] += u + v;
           if constexpr (C::BF) {
             w[i] = pack_bf16(u, v);
