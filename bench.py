@@ -12,7 +12,10 @@ configurations.  L2 is flushed (a 512 MiB write) before every timed step,
 outside the timed events.
 
 Prints one JSON line.  ``value`` = paged-decode KV-read GB/s over the whole step
-(algorithmic decode bytes / step time); ``roofline`` is for the decode kernel
+(algorithmic decode bytes / step time; the step -- the same library calls -- is
+captured once in a CUDA graph and replayed, as a serving loop replays its decode
+step; ``eager_ms_per_step`` times the calls issued one by one from Python);
+``roofline`` is for the decode kernel
 alone (profiling events on its launch stream); ``e2e`` repeats the step from
 pinned host buffers with the host<->device copies inside the timed region;
 ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same
@@ -282,8 +285,23 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": float(np.nanmax([num(r[3]) for r in rows]))}
 
 
-def time_steps(st, K, flush, partition_size, ws, profile=False):
-    """Per-step device time (ms) of K steps, L2 flushed before each (outside the events)."""
+def capture_step(st, partition_size, ws):
+    """The step (write + attention) captured once in a CUDA graph: replaying it issues the
+    same library launches, with their programmatic-launch edges, without per-launch host
+    work -- the way a serving loop replays its decode step."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run_step(st, partition_size, ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_steps(st, K, flush, partition_size, ws, profile=False, graph=None):
+    """Per-step device time (ms) of K steps, L2 flushed before each (outside the events);
+    with `graph`, each step is a replay of the captured step."""
     import paged_decode_attention_reshape_gb300 as pa
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if profile:
@@ -295,7 +313,10 @@ def time_steps(st, K, flush, partition_size, ws, profile=False):
         flush()
         ev[i][0].record()
         torch.cuda.nvtx.range_push("step")
-        run_step(st, partition_size, ws)
+        if graph is not None:
+            graph.replay()
+        else:
+            run_step(st, partition_size, ws)
         torch.cuda.nvtx.range_pop()
         ev[i][1].record()
     torch.cuda.synchronize()
@@ -530,12 +551,18 @@ def main(argv=None):
                 flush()
                 run_step(st, args.partition_size, wspace)
             torch.cuda.synchronize()
+    graph = capture_step(st, args.partition_size, wspace)
+    for _ in range(3):
+        flush()
+        graph.replay()
     barrier(ws)
     torch.cuda.synchronize()
     t0 = time.time()
-    step_ms, _ = time_steps(st, args.steps, flush, args.partition_size, wspace, profile=False)
+    step_ms, _ = time_steps(st, args.steps, flush, args.partition_size, wspace, profile=False, graph=graph)
     t1 = time.time()
     barrier(ws)
+    # the same steps launched one call at a time from Python (reported beside the graph time)
+    eager_ms, _ = time_steps(st, args.steps, flush, args.partition_size, wspace, profile=False)
     # per-kernel device times: the same steps again with the library's profiling events
     # around each launch (kept out of the step timing above: an event between the write and
     # the decode would hold back the decode's programmatic early launch)
@@ -549,6 +576,8 @@ def main(argv=None):
 
     ms = float(np.mean(step_ms))
     ms = max_over_ranks(ms, ws)
+    eager = max_over_ranks(float(np.mean(eager_ms)), ws)
+    pct = [float(x) for x in np.percentile(step_ms, [10, 50, 90])]
     dec_bytes = w.decode_bytes()
     value = job_throughput(dec_bytes, ws, ms)
     wr_ms, wr_n = prof[pa.PA_KERNEL_WRITE]
@@ -592,6 +621,9 @@ def main(argv=None):
                    "partition_tokens": P, "partitions_max": nparts, "parallelism": "replicas" if ws > 1 else "1 GPU"},
         "pct_of_hbm_peak": 100.0 * value / peak,
         "tokens_per_s": ws * w.S * w.nq / (ms * 1e-3),
+        "step_ms_p10_p50_p90": pct,
+        "launch": "step replayed from a CUDA graph (write + attention, programmatic-launch edge kept)",
+        "eager_ms_per_step": eager, "eager_value": job_throughput(dec_bytes, ws, eager),
         "decode_kernel_us": dk_avg * 1e3,
         "cache_write": {"GB/s": w.write_bytes() / ((wr_ms / max(1, wr_n)) * 1e-3) / 1e9,
                         "kernel_us": wr_ms / max(1, wr_n) * 1e3, "bytes": w.write_bytes()},

@@ -139,15 +139,6 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// True in exactly one lane of the (converged) warp.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
-      : "=r"(r)::"memory");
-  return r != 0;
-}
-
 // Shared memory matrix descriptor: 128-byte swizzle, start address, leading and stride
 // byte offsets (16-byte units), descriptor version 1.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -361,7 +352,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
           if (!__all_sync(0xffffffffu, umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort))) break;
           umma::fence_after();
           const uint64_t kd = kd0 + ((gs * C::GP * C::BOXB) >> 4);
-          if (umma::elect_one()) {
+          if (elect_one()) {
 #pragma unroll
             for (int j = 0; j < D / 16; ++j) {
               // 16-element k step j: box j / 4, 32 bytes per step within the 128-byte row
@@ -382,7 +373,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
               !__all_sync(0xffffffffu, umma_wait(pfull(0, bp), (kp >> 1) & 1, abort)))
             break;
           umma::fence_after();
-          if (umma::elect_one()) {
+          if (elect_one()) {
             for (int i = 0; i < npg; ++i) {
               const uint32_t phi = tt + 64u * bp + 16u * i;  // P hi: 8 columns, P lo: the next 8
               const uint64_t vd = vd0 + (((gsp * C::GP + i) * C::BOXB) >> 4);
@@ -396,7 +387,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
         }
       }
       if (*abort) {
-        if (umma::elect_one()) umma::commit(drain(t));  // every MMA of this issuer has completed once this arrives
+        if (elect_one()) umma::commit(drain(t));  // every MMA of this issuer has completed once this arrives
         __syncwarp();
         mbar_wait_bounded(drain(t), 0, kUmmaWaitLimit);
       }

@@ -98,7 +98,7 @@ struct MmaCfg {
 // already holds lane i's table entry for the warp's i-th page (read early by the
 // caller).  Returns true after a bad block id or a timed-out wait; `stalled` is set
 // on a timeout, after which the CTA must not issue into its stages again.
-template <int KIND, int D, int W, int STAGES>
+template <int KIND, int D, int W, int STAGES, bool PLAIN>
 __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
                                           const uint32_t sbase, uint8_t *const sgen, int &used, bool &stalled,
                                           const int s, const int len, const Cols &cm, const int pos0,
@@ -281,11 +281,20 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
     }
 
     // ---- online softmax (fragment: rows ra, ra+8 = tokens; columns 2qc, 2qc+1 = heads)
-    const int ta = page * kBlock + ra, tb = ta + 8;  // the fragment's two tokens
-    const float s0 = ta <= posA ? fmaf(ab0, static_cast<float>(ta - posA), (c0[0] + c1[0]) * sc0) : -INFINITY;
-    const float s1 = ta <= posB ? fmaf(ab1, static_cast<float>(ta - posB), (c0[1] + c1[1]) * sc1) : -INFINITY;
-    const float s2 = tb <= posA ? fmaf(ab0, static_cast<float>(tb - posA), (c0[2] + c1[2]) * sc0) : -INFINITY;
-    const float s3 = tb <= posB ? fmaf(ab1, static_cast<float>(tb - posB), (c0[3] + c1[3]) * sc1) : -INFINITY;
+    float s0, s1, s2, s3;
+    if constexpr (PLAIN) {  // one query token, no ALiBi: every column sees the tokens < len
+      const bool va = ra < nv, vb8 = ra + 8 < nv;
+      s0 = va ? (c0[0] + c1[0]) * sc0 : -INFINITY;
+      s1 = va ? (c0[1] + c1[1]) * sc1 : -INFINITY;
+      s2 = vb8 ? (c0[2] + c1[2]) * sc0 : -INFINITY;
+      s3 = vb8 ? (c0[3] + c1[3]) * sc1 : -INFINITY;
+    } else {
+      const int ta = page * kBlock + ra, tb = ta + 8;  // the fragment's two tokens
+      s0 = ta <= posA ? fmaf(ab0, static_cast<float>(ta - posA), (c0[0] + c1[0]) * sc0) : -INFINITY;
+      s1 = ta <= posB ? fmaf(ab1, static_cast<float>(ta - posB), (c0[1] + c1[1]) * sc1) : -INFINITY;
+      s2 = tb <= posA ? fmaf(ab0, static_cast<float>(tb - posA), (c0[2] + c1[2]) * sc0) : -INFINITY;
+      s3 = tb <= posB ? fmaf(ab1, static_cast<float>(tb - posB), (c0[3] + c1[3]) * sc1) : -INFINITY;
+    }
     // The running max of a head moves only when a score exceeds it by more than
     // kMaxSlack (log2 units); otherwise the page is weighted against the stale max,
     // p = 2^(s - m) <= 2^kMaxSlack, and the cross-lane max reduction and the rescale
@@ -472,7 +481,9 @@ __device__ __forceinline__ void zero_rows(const DecodeParams &p, const Cols &cm,
   }
 }
 
-template <int KIND, int D, int W, int STAGES>
+// PLAIN: one query token per sequence and no ALiBi (pa_decode), compiled without the
+// per-column causal limits and the bias.
+template <int KIND, int D, int W, int STAGES, bool PLAIN>
 __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
@@ -617,7 +628,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
       const int zlen = __ldg(p.seq_lens + z);
       bool bad = true;
       if (!dead)
-        bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, zlen, cm, zlen - 1, ng,
+        bad = run_pages<KIND, D, W, STAGES, PLAIN>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, zlen, cm, zlen - 1, ng,
                                             x - ps, y - ps, 0, false, pol);
       const bool any_bad = __syncthreads_or(bad);
       if (any_bad) dead = __syncthreads_or(stalled) || dead;
@@ -697,7 +708,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     return;
   }
 
-  const bool bad = run_pages<KIND, D, W, STAGES>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, cm, pos0, ng,
+  const bool bad = run_pages<KIND, D, W, STAGES, PLAIN>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, cm, pos0, ng,
                                                  pb, pe, pid_reg, true, pol);
   const bool any_bad = __syncthreads_or(bad);
 
@@ -748,24 +759,29 @@ struct MmaLaunch {
   using C = MmaCfg<KIND, D, W, ST>;
   static_assert(C::SMEM == mma_smem(KIND, D), "shape table out of sync");
 
+  template <bool PLAIN>
   static cudaError_t attrs() {
-    auto kern = decode_mma_kernel<KIND, D, W, ST>;
+    auto kern = decode_mma_kernel<KIND, D, W, ST, PLAIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     // same shared/L1 split as the cache write that usually precedes it (no reconfiguration)
     return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   }
   static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
-    cudaError_t e = attrs();
+    const bool plain = !p.qsl && !p.alibi;
+    cudaError_t e = plain ? attrs<true>() : attrs<false>();
     if (e != cudaSuccess) return e;
     const dim3 grid = p.flat > 0 ? dim3(p.flat, p.Hkv * p.HG, 1) : dim3(p.max_parts, p.Hkv * p.HG, p.S);
-    e = launch_pdl(decode_mma_kernel<KIND, D, W, ST>, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p, tmK, tmV);
+    e = plain ? launch_pdl(decode_mma_kernel<KIND, D, W, ST, true>, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p,
+                           tmK, tmV)
+              : launch_pdl(decode_mma_kernel<KIND, D, W, ST, false>, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p,
+                           tmK, tmV);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   static int occupancy() {  // 0 when it cannot be queried
     int n = 0;
-    if (attrs() != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<KIND, D, W, ST>, C::THREADS, C::SMEM) !=
+    if (attrs<false>() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<KIND, D, W, ST, false>, C::THREADS, C::SMEM) !=
             cudaSuccess)
       return 0;
     return n;
