@@ -99,3 +99,47 @@ def test_step_in_a_cuda_graph():
             c.Vval[s][L - 1] = V[s].double().numpy()
         c.q = q
         assert_close(g.out.double().cpu().numpy(), reference(c), "graph replay %d" % it)
+
+
+def _draw_varlen(rng):
+    """A varlen batch whose chunks reach both kernels: query columns per KV head (max new
+    tokens x G) from a few (column groups) to several hundred (query tiles, one or two per CTA)."""
+    D = int(rng.choice([64, 128]))
+    dt = torch.bfloat16 if rng.random() < 0.7 else torch.float16
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 5, 8]))
+    S = int(rng.integers(1, 5))
+    long_chunks = rng.random() < 0.7
+    cap = int(rng.choice([24, 48, 96])) if long_chunks else 6
+    lens, nqs = [], []
+    for _ in range(S):
+        L = int(rng.integers(1, 1200))
+        hi = min(L, cap)
+        n = int(rng.integers(0, hi + 1))
+        if long_chunks and rng.random() < 0.2:
+            n = L  # a whole prompt
+        lens.append(L)
+        nqs.append(n)
+    alibi = list(2.0 ** (-8.0 * np.arange(1, Hkv * G + 1) / (Hkv * G))) if rng.random() < 0.3 else None
+    nhd = bool(rng.random() < 0.3)
+    P = int(rng.choice([-1, 0, 64]))
+    return dict(lens=lens, nqs=nqs, Hq=Hkv * G, Hkv=Hkv, D=D, dtype=dt, alibi=alibi, nhd=nhd), P
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_varlen_cases(seed):
+    from test_gpu_varlen import make_varlen, on_gpu
+    from test_gpu_varlen import reference as varlen_reference
+    from test_gpu_varlen import run as varlen_run
+    rng = np.random.default_rng(2000 + seed)
+    kw, P = _draw_varlen(rng)
+    v = make_varlen(kw["lens"], kw["nqs"], kw["Hq"], kw["Hkv"], kw["D"], dtype=kw["dtype"], seed=seed,
+                    alibi=kw["alibi"], nhd=kw["nhd"])
+    g = on_gpu(v)
+    got = varlen_run(v, g, P)
+    rc, bits = pa.pa_check_device_error(g.err)
+    assert rc == 0, (rc, bits)
+    got = got.double().cpu().numpy()
+    assert not np.isnan(got).any()
+    cols = max(kw["nqs"] + [1]) * (kw["Hq"] // kw["Hkv"])
+    assert_close(got, varlen_reference(v), "seed %d: %s P=%d columns/KV head %d" % (seed, kw, P, cols))

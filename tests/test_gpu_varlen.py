@@ -29,11 +29,11 @@ class Varlen:
     pass
 
 
-def make_varlen(lens, nqs, Hq, Hkv, D, dtype=torch.bfloat16, fp8=False, seed=0, alibi=None, nq_max=None):
+def make_varlen(lens, nqs, Hq, Hkv, D, dtype=torch.bfloat16, fp8=False, seed=0, alibi=None, nq_max=None, nhd=False):
     """Caches for sequences of visible length lens[s] (history + new tokens), nqs[s] new query
     tokens each, packed in q [sum(nqs), Hq, D]."""
     c = make_case(len(lens), Hq, Hkv, D, lens, dtype=dtype, fp8=fp8, seed=seed,
-                  k_scale=0.05 if fp8 else 1.0, v_scale=0.07 if fp8 else 1.0, alibi=alibi)
+                  k_scale=0.05 if fp8 else 1.0, v_scale=0.07 if fp8 else 1.0, alibi=alibi, nhd=nhd)
     v = Varlen()
     v.c = c
     v.nqs = list(nqs)
