@@ -114,9 +114,31 @@ def stage(w, device="cuda", history=True, poison=True) -> Staged:
     st.qsl = torch.arange(0, w.S * w.nq + 1, w.nq, dtype=torch.int32, device=device) if w.nq > 1 else None
     st.k_step, st.v_step = data.step_rows(w, device)
     st.slot_mapping = torch.from_numpy(w.step_slot.astype(np.int64)).to(device)
+    st.new_rows_start = new_rows_start(w, device)
     if history:
         write_history(st, device)
     return st
+
+
+def new_rows_start(w, device="cuda"):
+    """How the step's rows map to sequences for pa_decode_step: None when row s is sequence
+    s's newest token, an int32 [S+1] tensor when each sequence's rows are its newest tokens in
+    order, sequence after sequence (c5's chunk), and False when the step's rows are not its
+    sequences' newest tokens (then the write and the attention are two calls)."""
+    if w.nq != 1:
+        return False
+    seqs, pos = np.asarray(w.step_seq), np.asarray(w.step_pos)
+    if len(seqs) == w.S and np.array_equal(seqs, np.arange(w.S)) and np.array_equal(pos, w.seq_lens - 1):
+        return None
+    counts = np.bincount(seqs, minlength=w.S)
+    start = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    if not np.all(np.diff(seqs) >= 0):
+        return False
+    for s in range(w.S):
+        n = int(counts[s])
+        if not np.array_equal(pos[start[s]:start[s + 1]], np.arange(int(w.seq_lens[s]) - n, int(w.seq_lens[s]))):
+            return False
+    return torch.from_numpy(start).to(device)
 
 
 def write_history(st: Staged, device="cuda", rows_per_call=1 << 16) -> None:
@@ -181,8 +203,21 @@ def run_decode(st: Staged, partition_size: int = 0, ws=None, out=None) -> None:
 
 
 def run_step(st: Staged, partition_size: int = 0, ws=None) -> None:
-    run_write(st)
-    run_decode(st, partition_size, ws)
+    """One step of the hot path: the cache write of the step's rows, then attention.  A decode
+    step whose rows are its sequences' newest tokens goes through pa_decode_step (one call; the
+    decode reads the untouched pages while the write runs); otherwise two calls."""
+    import paged_decode_attention_reshape_gb300 as pa
+    nrs = getattr(st, "new_rows_start", False)
+    if nrs is False:
+        run_write(st)
+        run_decode(st, partition_size, ws)
+        return
+    w = st.w
+    ks, vs = (st.k_scale, st.v_scale) if st.fp8 else (None, None)
+    pa.pa_decode_step(st.out, st.q, st.k_step, st.v_step, st.k_cache, st.v_cache, st.slot_mapping, st.block_table,
+                      st.seq_lens, w.scale, w.Hkv, new_rows_start=nrs, k_scale=ks, v_scale=vs,
+                      scale_stride=st.scale_stride, alibi_slopes=st.alibi, partition_size=partition_size,
+                      workspace=ws, device_error=st.err)
 
 
 # ------------------------------------------------------------ measurement
@@ -336,7 +371,8 @@ def e2e_steps(st, K, flush, partition_size, ws):
     staging buffer (one H2D copy), the library runs on views of it, and the output comes
     back with one D2H copy, all inside the timed events."""
     import copy
-    names = E2E_INPUTS + (("qsl",) if st.qsl is not None else ())
+    names = E2E_INPUTS + (("qsl",) if st.qsl is not None else ()) + \
+        (("new_rows_start",) if isinstance(getattr(st, "new_rows_start", None), torch.Tensor) else ())
     offs, off = {}, 0
     for n in names:
         t = getattr(st, n)

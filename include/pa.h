@@ -292,6 +292,35 @@ int pa_attention_varlen(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_c
                         pa_stream_t stream);
 
 /*
+ * pa_decode_step -- one decode step in one call: the cache write of the step's new rows
+ * (pa_reshape_and_cache_opt) followed by pa_decode_opt over the updated cache, with the
+ * decode reading everything the write does not touch while the write still runs.
+ *
+ * The pages call the two operations in this order for every layer ("How vLLM CUDA Kernels
+ * Write and Read the Paged KV Cache": the new token's K/V go to their slot, then attention
+ * reads the sequence's blocks through block_table).  Here the decode is launched behind the
+ * write with a programmatic dependency and waits for the write only before it reads a page
+ * that holds one of the new positions, and before it writes out or its workspace.
+ *
+ *   out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, opt: as
+ *                    pa_decode_opt (one query token per sequence; opt's scales and
+ *                    scale_stride also quantise the rows written to an FP8 cache).
+ *   key, value       [T, Hkv, D] new rows, slot_mapping int64 [T]: as pa_reshape_and_cache
+ *                    (kv dtype: E4M3 when the cache is E4M3, else the cache keeps q's dtype).
+ *   new_rows_start   NULL: T == S and row s is sequence s's newest token.  Else int32 [S + 1]
+ *                    (device): rows new_rows_start[s] .. new_rows_start[s+1]-1 are sequence
+ *                    s's newest n_s tokens, row i at position seq_lens[s] - n_s + i.
+ * Precondition (not checked on the device): every row's slot is the one its position maps to
+ * in its sequence's block table (or < 0: no write), and no other sequence of the batch reads
+ * that block.  Every argument of both operations is validated before anything is launched;
+ * the results equal those of the two calls made one after the other.
+ */
+int pa_decode_step(pa_tensor *out, const pa_tensor *q, const pa_tensor *key, const pa_tensor *value,
+                   pa_tensor *k_cache, pa_tensor *v_cache, const pa_tensor *slot_mapping,
+                   const pa_tensor *new_rows_start, const pa_tensor *block_table, const pa_tensor *seq_lens,
+                   float scale, int num_kv_heads, const pa_decode_options *opt, pa_stream_t stream);
+
+/*
  * pa_decode_noalloc -- pa_decode_ex for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this call; it exists for callers that have no

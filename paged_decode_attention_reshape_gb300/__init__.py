@@ -30,7 +30,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED_DTYPE", 
           -8: "PA_ERR_DEVICE_TIMEOUT", -9: "PA_ERR_NO_BLOCKS"}
 
 EXPORTS = ("pa_reshape_and_cache", "pa_reshape_and_cache_opt", "pa_decode", "pa_decode_ex", "pa_decode_opt",
-           "pa_attention_varlen", "pa_decode_noalloc", "pa_decode_plan", "pa_decode_workspace_size", "pa_check_device_error",
+           "pa_attention_varlen", "pa_decode_step", "pa_decode_noalloc", "pa_decode_plan", "pa_decode_workspace_size", "pa_check_device_error",
            "pa_status_string", "pa_profile_enable", "pa_profile_read", "pa_bm_create", "pa_bm_destroy",
            "pa_bm_num_free", "pa_bm_block_refs", "pa_bm_seq_len", "pa_bm_append", "pa_bm_fork", "pa_bm_free",
            "pa_bm_export", "pa_copy_blocks")
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
             L.pa_reshape_and_cache_opt.argtypes = [T, T, T, T, T, i32, ctypes.POINTER(PaWriteOptions), P]
             L.pa_decode_opt.restype = i32
             L.pa_decode_opt.argtypes = [T, T, T, T, T, T, f32, i32, ctypes.POINTER(PaDecodeOptions), P]
+            L.pa_decode_step.restype = i32
+            L.pa_decode_step.argtypes = [T, T, T, T, T, T, T, T, T, T, f32, i32, ctypes.POINTER(PaDecodeOptions), P]
             L.pa_attention_varlen.restype = i32
             L.pa_attention_varlen.argtypes = [T, T, T, T, T, T, T, f32, i32, i32, ctypes.POINTER(PaDecodeOptions), P]
             i64p = ctypes.POINTER(ctypes.c_int64)
@@ -209,6 +211,26 @@ def pa_decode_opt(out, q, k_cache, v_cache, block_table, seq_lens, scale: float,
     rc = lib().pa_decode_opt(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), ctypes.byref(o),
                              _stream(stream))
     _check(rc, "pa_decode_opt")
+
+
+def pa_decode_step(out, q, key, value, k_cache, v_cache, slot_mapping, block_table, seq_lens, scale: float,
+                   num_kv_heads: int, new_rows_start=None, k_scale=None, v_scale=None, scale_stride: int = 0,
+                   alibi_slopes=None, partition_size: int = 0, workspace=None, device_error=None,
+                   stream=None) -> None:
+    """The cache write of the step's new rows (key / value [T, Hkv, D] to slot_mapping) and the
+    decode over the updated cache in one call; the decode reads everything but the new
+    positions while the write runs.  new_rows_start: None (row s = sequence s's newest token)
+    or int32 [S+1] (rows of sequence s, its newest tokens in order).  Options as pa_decode_opt;
+    the scales also quantise the rows written to an FP8 cache."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    o = PaDecodeOptions(_ptr(k_scale), _ptr(v_scale), int(scale_stride), _ptr(alibi_slopes), int(partition_size),
+                        _ptr(workspace), ws_bytes, _ptr(device_error))
+    nrs = None if new_rows_start is None else ctypes.byref(desc(new_rows_start))
+    args = (desc(out), desc(q), desc(key), desc(value), desc(k_cache), desc(v_cache), desc(slot_mapping))
+    rc = lib().pa_decode_step(*[ctypes.byref(a) for a in args], nrs, ctypes.byref(desc(block_table)),
+                              ctypes.byref(desc(seq_lens)), float(scale), int(num_kv_heads), ctypes.byref(o),
+                              _stream(stream))
+    _check(rc, "pa_decode_step")
 
 
 def pa_attention_varlen(out, q, k_cache, v_cache, query_start_loc, block_table, seq_lens, scale: float,

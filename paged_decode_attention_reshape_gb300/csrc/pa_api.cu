@@ -462,7 +462,8 @@ namespace {
 int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                 const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
                 const pa_decode_options &o, bool internal_ws, pa_stream_t stream,
-                const pa_tensor *query_start_loc = nullptr, int max_query_len = 1) {
+                const pa_tensor *query_start_loc = nullptr, int max_query_len = 1,
+                const pa_tensor *new_rows_start = nullptr, bool early = false, bool dry = false) {
   const float *k_scale = o.k_scale, *v_scale = o.v_scale;
   const int partition_size = o.partition_size;
   void *workspace = o.workspace;
@@ -500,6 +501,12 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED_SHAPE;
   if ((kind == KIND_FP8_BF16Q || kind == KIND_FP8_F16Q) && D < 128) return PA_ERR_UNSUPPORTED_SHAPE;
   if (S64 > 65535 || Hq64 > 65535 || block_table->shape[1] > (INT32_MAX / kBlock)) return PA_ERR_UNSUPPORTED_SHAPE;
+  if (early && new_rows_start) {
+    if ((r = check_desc(new_rows_start, 1))) return r;
+    if (new_rows_start->dtype != PA_I32) return PA_ERR_UNSUPPORTED_DTYPE;
+    if (new_rows_start->shape[0] != S64 + 1 || new_rows_start->stride[0] != 1) return PA_ERR_INVALID_ARG;
+    if (S64 > 0 && !new_rows_start->data) return PA_ERR_INVALID_ARG;
+  }
   if (S64 == 0 || q->shape[0] == 0) return PA_OK;
   if (!q->data || !out->data || !block_table->data || !seq_lens->data) return PA_ERR_INVALID_ARG;
   const int qb = elem_bytes(q->dtype);
@@ -556,6 +563,8 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   p.max_parts = max_parts;
   p.cluster = pl.cluster;
   p.flat = pl.flat;
+  p.early = early && !varlen ? 1 : 0;
+  p.new_start = p.early && new_rows_start ? static_cast<const int32_t *>(new_rows_start->data) : nullptr;
   p.err = device_error;
   {
     // Order the batch longest-first only when its CTAs cannot all be resident at once:
@@ -569,6 +578,14 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   if (kind != KIND_FP8_BF16Q && kind != KIND_FP8_F16Q) p.k_scale = p.v_scale = nullptr;
   if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
 
+  if (dry) {  // validation only (pa_decode_step checks everything before its first launch)
+    if (((max_parts > 1 && pl.cluster <= 1) || pl.flat > 0) && !internal_ws) {
+      const WsLayout lay = workspace_layout(S, Hqv, Hkv, D, maxNB, P, pl.flat);
+      if (!workspace || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+      if (!aligned16(workspace)) return PA_ERR_ALIGNMENT;
+    }
+    return PA_OK;
+  }
   if ((max_parts > 1 && pl.cluster <= 1) || pl.flat > 0) {
     const WsLayout lay = workspace_layout(S, Hqv, Hkv, D, maxNB, P, pl.flat);
     if (internal_ws) {
@@ -660,6 +677,28 @@ PA_API int pa_attention_varlen(pa_tensor *out, const pa_tensor *q, const pa_tens
   const bool internal = !o.workspace && o.workspace_bytes == 0;
   return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, internal, stream,
                      query_start_loc, max_query_len);
+}
+
+PA_API int pa_decode_step(pa_tensor *out, const pa_tensor *q, const pa_tensor *key, const pa_tensor *value,
+                          pa_tensor *k_cache, pa_tensor *v_cache, const pa_tensor *slot_mapping,
+                          const pa_tensor *new_rows_start, const pa_tensor *block_table, const pa_tensor *seq_lens,
+                          float scale, int num_kv_heads, const pa_decode_options *opt, pa_stream_t stream) {
+  const pa_decode_options o = opt ? *opt : pa_decode_options{};
+  const bool internal = !o.workspace && o.workspace_bytes == 0;
+  int r;
+  if ((r = check_desc(q, 3)) || (r = check_desc(key, 3)) || (r = check_desc(k_cache, 4))) return r;
+  if (!new_rows_start && key->shape[0] != q->shape[0]) return PA_ERR_INVALID_ARG;  // one new row per sequence
+  if (new_rows_start && ((r = check_desc(new_rows_start, 1)) || new_rows_start->shape[0] != q->shape[0] + 1))
+    return r ? r : PA_ERR_INVALID_ARG;
+  // every argument of both halves is checked before anything is launched
+  if ((r = decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, internal, stream,
+                       nullptr, 1, new_rows_start, true, true)))
+    return r;
+  const pa_write_options wo{o.k_scale, o.v_scale, o.scale_stride, o.device_error};
+  const int kv = k_cache->dtype == PA_FP8_E4M3 ? PA_KV_FP8_E4M3 : PA_KV_AUTO;
+  if ((r = pa_reshape_and_cache_opt(key, value, k_cache, v_cache, slot_mapping, kv, &wo, stream))) return r;
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, internal, stream,
+                     nullptr, 1, new_rows_start, true);
 }
 
 PA_API int pa_check_device_error(int *device_error, int *bits_out, pa_stream_t stream) {

@@ -103,7 +103,7 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
                                           const uint32_t sbase, uint8_t *const sgen, int &used, bool &stalled,
                                           const int s, const int len, const Cols &cm, const int pos0,
                                           const int ng, const int pb, const int pe, int pid_reg,
-                                          const bool pid_ready, const uint64_t pol) {
+                                          const bool pid_ready, const uint64_t pol, const int wait_page) {
   using C = MmaCfg<KIND, D, W, STAGES>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = cm.g;
@@ -114,7 +114,12 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
   const int u0 = used;
   bool bad = false;
 
+  bool waited = false;  // early reads: this warp has waited for the preceding write grid
   auto issue = [&](int kk) {  // whole warp; kk increases by one per call
+    if (!waited && pb + warp + kk * W >= wait_page) {  // a page that may hold new positions
+      grid_dependency_wait();
+      waited = true;
+    }
     if ((kk & 31) == 0 && (kk > 0 || !pid_ready)) {
       const int k2 = kk + lane;
       pid_reg = (k2 < nmine) ? __ldg(bt + pb + warp + k2 * W) : 0;
@@ -543,7 +548,9 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
       }
     }
   }
-  grid_dependency_wait();
+  // Early reads apply to the one-unit path only (the balanced and cluster splits wait here).
+  const bool early = p.early && !flat && p.cluster <= 1;
+  if (!early) grid_dependency_wait();
 
   // Pages are read once per CTA: evict them first.  (With several column groups of one KV
   // head reading the same pages, evict-normal measured 3 % slower on GB300: 4 query tokens
@@ -629,7 +636,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
       bool bad = true;
       if (!dead)
         bad = run_pages<KIND, D, W, STAGES, PLAIN>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, zlen, cm, zlen - 1, ng,
-                                            x - ps, y - ps, 0, false, pol);
+                                            x - ps, y - ps, 0, false, pol, 0);
       const bool any_bad = __syncthreads_or(bad);
       if (any_bad) dead = __syncthreads_or(stalled) || dead;
       if (x == ps && y == pn) {
@@ -704,12 +711,22 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     pe = min(npages, pb + p.pages_per_part);
   }
   if (pb >= pe && !clustered) {  // (an empty cluster rank stays: it takes part in the merge)
-    if (npages == 0 && part == 0) zero_rows<OutT>(p, cm, ng, D, C::THREADS);  // empty sequence (any split)
+    if (npages == 0 && part == 0) {  // empty sequence (any split)
+      if (early) grid_dependency_wait();
+      zero_rows<OutT>(p, cm, ng, D, C::THREADS);
+    }
     return;
+  }
+  // early reads: pages from the first new position on wait for the preceding write grid
+  int wait_page = 0;
+  if (early) {
+    const int nnew = p.new_start ? __ldg(p.new_start + s + 1) - __ldg(p.new_start + s) : 1;
+    wait_page = nnew <= 0 ? 0x7fffffff : max(0, len - nnew) / kBlock;
   }
 
   const bool bad = run_pages<KIND, D, W, STAGES, PLAIN>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, cm, pos0, ng,
-                                                 pb, pe, pid_reg, true, pol);
+                                                 pb, pe, pid_reg, true, pol, wait_page);
+  if (early) grid_dependency_wait();  // before any output or workspace write
   const bool any_bad = __syncthreads_or(bad);
 
   if (clustered) {

@@ -66,6 +66,13 @@ struct DecodeParams {
   int64_t Tq;                          // rows of q / out
   int VH;                              // virtual heads per KV head; HG = ceil(VH / 8)
   int nhd;                             // caches token-major within a block (TMA coordinates (d, g, 0, blk))
+  // Early reads (pa_decode_step): the grid launched just before this one writes only the
+  // newest n_s positions of each sequence s (n_s = new_start[s+1] - new_start[s], or 1 when
+  // new_start is null).  The kernel then reads q, the tables and every other page before that
+  // grid completes and waits for it only before a page holding new positions and before
+  // writing any output.  0: wait for it first.
+  int early;
+  const int32_t *new_start;
   int flat;                            // > 0: balanced split, this many CTAs per head row (S <= kFlatMaxSeqs)
   // fp32 path only: direct cache pointers and strides (elements)
   const float *kc, *vc;
