@@ -19,20 +19,23 @@
 //   O[128 x D] += P[128 x 16] . V_page[16 x D]  tcgen05.mma per page and half, A = P from
 //                                               TMEM, B = the V page in shared memory
 // Roles (T tiles): warps 0 .. 4T-1 run the softmax and the epilogue (warp w belongs to
-// tile w / 4 and owns its TMEM lanes and rows 32 (w % 4) ..), warp 4T allocates TMEM and
-// its lane 0 issues the MMAs of every tile, warp 4T+1 resolves block_table and issues the
-// TMA page loads into a ring of R page slots.
+// tile w / 4 and owns its TMEM lanes and rows 32 (w % 4) ..); warp 4T + t issues the MMAs
+// of tile t (the whole warp runs the loop, one elected lane issues), warp 4T also allocates
+// TMEM; warp 5T resolves block_table and issues the TMA page loads into a ring of R page
+// slots.
 // Shared memory holds Q (loaded by the softmax threads, 128-byte swizzle) and the K and V
 // rings, one region per 64-element box of a row, so that the 16-token pages of a group
 // sit at one 1024-byte stride per 8 rows and form one MMA operand.  S and P of groups k
 // and k + 1 use two TMEM buffers; O lives in TMEM until the epilogue normalises it.
 //
 // Synchronisation (mbarriers, every wait bounded and abandoned when another role gave
-// up): full[slot] (TMA bytes) -> MMA; s_full[b] (commit) -> softmax; p_full[b] (128
-// arrivals) -> MMA; o_done (commit after each group's P.V) -> softmax, which waits for
-// every group in turn (an O rescale needs it, and the parity waits stay one phase apart);
-// empty[slot] (commit) -> TMA.  MMAs issued by one thread run in order, so S of group
-// k + 2 may overwrite the P that P.V of group k reads.
+// up): full[slot] (TMA bytes) -> the issuers; per tile s_full[b] (commit) -> softmax,
+// p_full[b] (128 arrivals) -> its issuer, o_done (commit after each group's P.V) ->
+// softmax, which waits for every group in turn (an O rescale needs it, and the parity
+// waits stay one phase apart); empty[slot] (one commit per active tile) -> TMA.  The MMAs
+// of one issuer run in order, so S of group k + 2 may overwrite the P that P.V of group k
+// reads.  Tile 0 zeroes the V rows past the sequence in the last page before it hands over
+// its P; the other tiles' last P.V also waits for that hand-over.
 #pragma once
 
 #include "pa_device.cuh"
