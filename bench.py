@@ -130,6 +130,8 @@ def new_rows_start(w, device="cuda"):
     seqs, pos = np.asarray(w.step_seq), np.asarray(w.step_pos)
     if len(seqs) == w.S and np.array_equal(seqs, np.arange(w.S)) and np.array_equal(pos, w.seq_lens - 1):
         return None
+    if len(seqs) == 0 or seqs.min() < 0:   # a row of no sequence (padding tagged -1)
+        return False
     counts = np.bincount(seqs, minlength=w.S)
     start = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     if not np.all(np.diff(seqs) >= 0):
