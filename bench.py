@@ -352,6 +352,11 @@ def time_steps(st, K, flush, partition_size, ws, profile=False, graph=None):
         torch.cuda.nvtx.range_push("step")
         if graph is not None:
             graph.replay()
+        elif profile:
+            # per-kernel times: the write and the attention as two calls, so the attention
+            # kernel's time is its own (in pa_decode_step it starts early, while the write runs)
+            run_write(st)
+            run_decode(st, partition_size, ws)
         else:
             run_step(st, partition_size, ws)
         torch.cuda.nvtx.range_pop()

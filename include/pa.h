@@ -299,8 +299,11 @@ int pa_attention_varlen(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_c
  * The pages call the two operations in this order for every layer ("How vLLM CUDA Kernels
  * Write and Read the Paged KV Cache": the new token's K/V go to their slot, then attention
  * reads the sequence's blocks through block_table).  Here the decode is launched behind the
- * write with a programmatic dependency and waits for the write only before it reads a page
- * that holds one of the new positions, and before it writes out or its workspace.
+ * write with a programmatic dependency.  With new_rows_start (several new rows per
+ * sequence) it reads q, the tables and every page without a new position while the write
+ * runs, and waits for the write only before a page that holds new positions and before it
+ * writes out or its workspace; with one new row per sequence it starts behind the write as
+ * pa_decode_opt does (the write is over before early reads could help).
  *
  *   out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, opt: as
  *                    pa_decode_opt (one query token per sequence; opt's scales and

@@ -65,6 +65,7 @@ namespace pa {
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before a wait gives up (>= ~20 ms)
 constexpr float kMaxSlack = 8.f;            // log2 units: probabilities within a page stay <= 256
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kNoWaitPage = 0x7fffffff;     // run_pages: no page waits for the preceding grid
 constexpr float kEmptyMax = -1e30f;         // running max of a column with no visible token yet
 
 template <int KIND, int D, int W, int STAGES>
@@ -98,7 +99,7 @@ struct MmaCfg {
 // already holds lane i's table entry for the warp's i-th page (read early by the
 // caller).  Returns true after a bad block id or a timed-out wait; `stalled` is set
 // on a timeout, after which the CTA must not issue into its stages again.
-template <int KIND, int D, int W, int STAGES, bool PLAIN>
+template <int KIND, int D, int W, int STAGES, bool PLAIN, bool EARLY>
 __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV,
                                           const uint32_t sbase, uint8_t *const sgen, int &used, bool &stalled,
                                           const int s, const int len, const Cols &cm, const int pos0,
@@ -116,9 +117,11 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
 
   bool waited = false;  // early reads: this warp has waited for the preceding write grid
   auto issue = [&](int kk) {  // whole warp; kk increases by one per call
-    if (!waited && pb + warp + kk * W >= wait_page) {  // a page that may hold new positions
-      grid_dependency_wait();
-      waited = true;
+    if constexpr (EARLY) {
+      if (!waited && pb + warp + kk * W >= wait_page) {  // a page that may hold new positions
+        grid_dependency_wait();
+        waited = true;
+      }
     }
     if ((kk & 31) == 0 && (kk > 0 || !pid_ready)) {
       const int k2 = kk + lane;
@@ -487,8 +490,10 @@ __device__ __forceinline__ void zero_rows(const DecodeParams &p, const Cols &cm,
 }
 
 // PLAIN: one query token per sequence and no ALiBi (pa_decode), compiled without the
-// per-column causal limits and the bias.
-template <int KIND, int D, int W, int STAGES, bool PLAIN>
+// per-column causal limits and the bias.  EARLY (with PLAIN only): the early reads of
+// pa_decode_step (DecodeParams::early); a wait inside the page loop costs the other
+// variants about 1.4 us on a 30 us decode, so only this one carries it.
+template <int KIND, int D, int W, int STAGES, bool PLAIN, bool EARLY>
 __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
@@ -549,7 +554,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     }
   }
   // Early reads apply to the one-unit path only (the balanced and cluster splits wait here).
-  const bool early = p.early && !flat && p.cluster <= 1;
+  const bool early = EARLY && p.early && !flat && p.cluster <= 1;
   if (!early) grid_dependency_wait();
 
   // Pages are read once per CTA: evict them first.  (With several column groups of one KV
@@ -635,8 +640,8 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
       const int zlen = __ldg(p.seq_lens + z);
       bool bad = true;
       if (!dead)
-        bad = run_pages<KIND, D, W, STAGES, PLAIN>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, zlen, cm, zlen - 1, ng,
-                                            x - ps, y - ps, 0, false, pol, 0);
+        bad = run_pages<KIND, D, W, STAGES, PLAIN, false>(p, &tmK, &tmV, sbase, sgen, used, stalled, z, zlen, cm, zlen - 1, ng,
+                                            x - ps, y - ps, 0, false, pol, kNoWaitPage);
       const bool any_bad = __syncthreads_or(bad);
       if (any_bad) dead = __syncthreads_or(stalled) || dead;
       if (x == ps && y == pn) {
@@ -718,13 +723,13 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
     return;
   }
   // early reads: pages from the first new position on wait for the preceding write grid
-  int wait_page = 0;
+  int wait_page = kNoWaitPage;
   if (early) {
     const int nnew = p.new_start ? __ldg(p.new_start + s + 1) - __ldg(p.new_start + s) : 1;
-    wait_page = nnew <= 0 ? 0x7fffffff : max(0, len - nnew) / kBlock;
+    wait_page = nnew <= 0 ? kNoWaitPage : max(0, len - nnew) / kBlock;
   }
 
-  const bool bad = run_pages<KIND, D, W, STAGES, PLAIN>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, cm, pos0, ng,
+  const bool bad = run_pages<KIND, D, W, STAGES, PLAIN, EARLY>(p, &tmK, &tmV, sbase, sgen, used, stalled, s, len, cm, pos0, ng,
                                                  pb, pe, pid_reg, true, pol, wait_page);
   if (early) grid_dependency_wait();  // before any output or workspace write
   const bool any_bad = __syncthreads_or(bad);
@@ -776,9 +781,9 @@ struct MmaLaunch {
   using C = MmaCfg<KIND, D, W, ST>;
   static_assert(C::SMEM == mma_smem(KIND, D), "shape table out of sync");
 
-  template <bool PLAIN>
+  template <bool PLAIN, bool EARLY>
   static cudaError_t attrs() {
-    auto kern = decode_mma_kernel<KIND, D, W, ST, PLAIN>;
+    auto kern = decode_mma_kernel<KIND, D, W, ST, PLAIN, EARLY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     // same shared/L1 split as the cache write that usually precedes it (no reconfiguration)
@@ -786,19 +791,22 @@ struct MmaLaunch {
   }
   static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
     const bool plain = !p.qsl && !p.alibi;
-    cudaError_t e = plain ? attrs<true>() : attrs<false>();
+    const bool early = plain && p.early;  // (the general variant ignores p.early: it waits first)
+    cudaError_t e = early ? attrs<true, true>() : plain ? attrs<true, false>() : attrs<false, false>();
     if (e != cudaSuccess) return e;
     const dim3 grid = p.flat > 0 ? dim3(p.flat, p.Hkv * p.HG, 1) : dim3(p.max_parts, p.Hkv * p.HG, p.S);
-    e = plain ? launch_pdl(decode_mma_kernel<KIND, D, W, ST, true>, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p,
-                           tmK, tmV)
-              : launch_pdl(decode_mma_kernel<KIND, D, W, ST, false>, grid, dim3(C::THREADS), C::SMEM, st, p.cluster, p,
-                           tmK, tmV);
+    const dim3 block(C::THREADS);
+    e = early   ? launch_pdl(decode_mma_kernel<KIND, D, W, ST, true, true>, grid, block, C::SMEM, st, p.cluster, p, tmK, tmV)
+        : plain ? launch_pdl(decode_mma_kernel<KIND, D, W, ST, true, false>, grid, block, C::SMEM, st, p.cluster, p, tmK, tmV)
+                : launch_pdl(decode_mma_kernel<KIND, D, W, ST, false, false>, grid, block, C::SMEM, st, p.cluster, p, tmK,
+                             tmV);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   static int occupancy() {  // 0 when it cannot be queried
     int n = 0;
-    if (attrs<false>() != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<KIND, D, W, ST, false>, C::THREADS, C::SMEM) !=
+    if (attrs<false, false>() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<KIND, D, W, ST, false, false>, C::THREADS,
+                                                      C::SMEM) !=
             cudaSuccess)
       return 0;
     return n;
