@@ -240,3 +240,32 @@ def test_negative_scale_stride_is_refused(L):
     w = pa.PaWriteOptions()
     w.scale_stride = -2
     assert L.pa_reshape_and_cache_opt(None, None, None, None, None, 0, ctypes.byref(w), None) == -1
+
+
+def _step(L, out, q, key, val, kc, vc, sm, nrs, bt, sl, hkv):
+    return L.pa_decode_step(ctypes.byref(out), ctypes.byref(q), ctypes.byref(key), ctypes.byref(val),
+                            ctypes.byref(kc), ctypes.byref(vc), ctypes.byref(sm),
+                            None if nrs is None else ctypes.byref(nrs), ctypes.byref(bt), ctypes.byref(sl), 0.125,
+                            hkv, None, None)
+
+
+def test_step_validation(L):
+    """pa_decode_step checks the decode's arguments and the row mapping before it launches
+    anything (the write's own checks come next, still before its launch)."""
+    S, Hq, Hkv, D, NB, MB = 3, 8, 2, 128, 16, 4
+    q = _t([S, Hq, D], pa.PA_BF16)
+    out = _t([S, Hq, D], pa.PA_BF16, ptr=0x20000)
+    kc = _t([NB, Hkv, 16, D], pa.PA_BF16)
+    vc = _t([NB, Hkv, 16, D], pa.PA_BF16)
+    bt = _t([S, MB], pa.PA_I32)
+    sl = _t([S], pa.PA_I32)
+    key = _t([S, Hkv, D], pa.PA_BF16)
+    val = _t([S, Hkv, D], pa.PA_BF16)
+    sm = _t([S], pa.PA_I64)
+    # one row per sequence unless new_rows_start says otherwise
+    assert _step(L, out, q, _t([S + 1, Hkv, D], pa.PA_BF16), _t([S + 1, Hkv, D], pa.PA_BF16), kc, vc,
+                 _t([S + 1], pa.PA_I64), None, bt, sl, Hkv) == -1
+    assert _step(L, out, q, key, val, kc, vc, sm, _t([S], pa.PA_I32), bt, sl, Hkv) == -1      # needs S + 1
+    assert _step(L, out, q, key, val, kc, vc, sm, _t([S + 1], pa.PA_I64), bt, sl, Hkv) == -2  # int32 only
+    assert _step(L, out, q, key, val, kc, vc, sm, None, bt, sl, 3) == -1                      # decode side
+    assert _step(L, out, _t([S, 7, D], pa.PA_BF16), key, val, kc, vc, sm, None, bt, sl, Hkv) == -1
