@@ -13,8 +13,10 @@
  *                          log-sum-exp reduce ("Inside vLLM CUDA Kernels", Part 3;
  *                          "vLLM 源码完全拆解（七）", 参数与内存布局 through V1 与 V2)
  *
+ *   pa_decode_step         the cache write and the decode of one step in one call
  *   pa_attention_varlen    several new query tokens per sequence, causal
- *                          ("Inside vLLM CUDA Kernels", Part 3, the varlen read path)
+ *                          ("Inside vLLM CUDA Kernels", Part 3, the varlen read path);
+ *                          long chunks run on a tcgen05 query-tile kernel
  *   pa_*_opt               the same calls with per-head FP8 scales and ALiBi
  *   pa_bm_*, pa_copy_blocks  host block manager and device block copy ("tiny-vllm,
  *                          Part 6"; "PagedAttention kernel: paged KV cache & block
