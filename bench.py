@@ -236,12 +236,38 @@ def _peaks(key="hbm_gbs"):
         return (FALLBACK_HBM_GBS if key == "hbm_gbs" else FALLBACK_BF16_TFLOPS_SUSTAINED), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and blank space (string literals kept), so an edit to a
+    comment does not count as a change of the kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':  # string literal, escapes included
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def decode_source_hash(sources=None) -> str:
+    """Hash of the kernel sources' code (comments and spacing ignored): ncu traffic taken at
+    another hash is reported as null."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_decode_attention_reshape_gb300", "csrc")
     for name in (sources or DECODE_SOURCES):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -53,7 +53,10 @@
 //
 // The kernel is launched as a programmatic dependent of the previous grid on the
 // stream: it waits for that grid before its first global read, so its launch
-// overlaps the previous kernel's tail.
+// overlaps the previous kernel's tail.  Three variants per shape: the general one
+// (several query tokens, ALiBi), PLAIN (one query token, no ALiBi: one compare per score
+// for the page tail), and PLAIN + EARLY for pa_decode_step's multi-row steps, which reads
+// everything but the pages with new positions before that wait.
 #pragma once
 
 #include "pa_device.cuh"
