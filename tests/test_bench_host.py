@@ -55,3 +55,14 @@ def test_query_tile_choice():
     assert not configs.get("c3-spec4").query_tile()   # 16 query columns per KV head
     assert not configs.get("c3").query_tile()
     assert not configs.get("c5").query_tile()         # one query token per sequence
+
+
+def test_source_hash_ignores_comments_and_spacing_only():
+    code = 'int a = 1;  // note\n/* block\n comment */ asm("mov.u32 %0, %1; // not a comment");\nint b;'
+    same = 'int a = 1;\n\n   asm("mov.u32 %0, %1; // not a comment"); int b;'
+    other = 'int a = 2; asm("mov.u32 %0, %1; // not a comment"); int b;'
+    lit = 'int a = 1; asm("mov.u32 %0, %1; // another literal"); int b;'
+    assert bench._code_only(code) == bench._code_only(same)
+    assert bench._code_only(code) != bench._code_only(other)
+    assert bench._code_only(code) != bench._code_only(lit)     # text inside a string literal counts
+    assert bench._code_only('s = "a \\" // b"; x;') == 's = "a \\" // b"; x;'
