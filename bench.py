@@ -543,8 +543,8 @@ def main_reference(args):
     if rank != 0:
         return 0
     w = configs.get(args.config)
-    budget = 150.0
-    per_step = max(1.0, min(6.0, budget / max(1, args.steps + args.warmup)))
+    total_cpu_s = 150.0   # host seconds the whole reference run may take
+    per_step = max(1.0, min(6.0, total_cpu_s / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         cpu_baseline(w, target_s=per_step / 3)
     vals = []
