@@ -435,13 +435,13 @@ def e2e_steps(st, K, flush, partition_size, ws):
     return [a.elapsed_time(b) for a, b in ev], h2d, d2h
 
 
-def cpu_baseline(w, target_s=12.0, max_seqs=None):
+def cpu_baseline(w, target_s=12.0, max_seqs=None, threads=None):
     """Time the fp64 CPU oracle (as it stands) on a bounded sample of the workload: the cache
     write of the sampled sequences' step rows and the dense decode of all their query heads.
-    Threads: one oracle call per (sequence) at a time on every host core."""
+    Threads: one oracle call per (sequence) at a time on every host core (or `threads`)."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
-    cores = len(os.sched_getaffinity(0))
+    cores = threads or len(os.sched_getaffinity(0))
     rng = np.random.default_rng(7)
     order = rng.permutation(w.S)
     qs = data.q(w, "cpu").float().double().numpy().reshape(w.S, w.nq, w.Hq, w.D)
@@ -683,6 +683,8 @@ def main(argv=None):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
+        if w.S <= 64 and w.nq == 1:   # the small decode workloads: one host thread as well
+            cpu["single_thread"] = cpu_baseline(w, target_s=4.0, threads=1)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
