@@ -195,6 +195,13 @@ int pa_decode(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, cons
 /*
  * pa_decode_ex -- pa_decode with every knob.
  *
+ * Split-KV ("vLLM 源码完全拆解（七）", V1 与 V2: why long contexts need partitions -- a
+ * small batch gives too few (sequence, head) work items to fill the GPU, so the context is
+ * cut into partitions computed in parallel whose partial results are rescaled and merged;
+ * "Inside vLLM CUDA Kernels", Part 3: split-KV changes the work partition, not the
+ * softmax identity).  The pages' fixed 512-token partition and 8192-token V1/V2 switch are
+ * replaced by a plan measured on GB300 (pa_decode_plan).
+ *
  *   k_scale, v_scale  device fp32 per-tensor dequantisation scales for an FP8 cache
  *                     (K and V element values are code_value * scale); NULL = 1.0.
  *   partition_size    how the KV range of a sequence is split: 0 = chosen by the
@@ -248,6 +255,13 @@ typedef struct {
     void *workspace;             /* as pa_decode_ex; NULL with 0 bytes = the library's */
     size_t workspace_bytes;      /*   internal workspace (pa_decode's) */
     int *device_error;           /* device int to OR error bits into, or NULL */
+    /* Poll limit of the first shared-memory pipeline wait (decode: each warp's first page;
+     * query tile: the first K/V group).  0 = the normal limit (about 2^20 polls); > 0 = that
+     * many polls; < 0 = give up without polling.  For testing the timeout path: a wait that
+     * gives up first waits (with the normal limit) for the copies it had in flight, sets
+     * PA_DEVERR_WAIT_TIMEOUT and writes no output for its work item (nor for a split-KV unit
+     * that any of its parts gave up on).  Every later wait keeps the normal limit. */
+    int first_wait_limit;
 } pa_decode_options;
 
 /*
@@ -359,6 +373,13 @@ int pa_decode_noalloc(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cac
 
 /*
  * pa_decode_plan -- host-only: the split pa_decode_ex would use.
+ *
+ * The pages choose between the unpartitioned kernel and 512-token partitions by a fixed
+ * rule (max_seq_len <= 8192 and one partition or num_seqs * num_heads > 512: unsplit) and
+ * describe the choice as a trade-off between parallelism and the extra reduction, to be
+ * weighed per shape ("vLLM 源码完全拆解（七）", V1 与 V2 and 性能模型).  This plan makes
+ * the same trade on GB300 from the batch's work units against the GPU's resident CTA slots,
+ * fitted to a measured sweep of partition sizes over the benchmark workloads.
  *   kv_dtype_code   pa_dtype of the cache; sm_count <= 0 queries the current device.
  *   partition_size  in: as for pa_decode_ex.  *partition_out: tokens per fixed
  *                   partition, 0 = unsplit, -C for the cluster split into C parts, or

@@ -57,7 +57,7 @@ class PaDecodeOptions(ctypes.Structure):
     _fields_ = [("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("scale_stride", ctypes.c_int64),
                 ("alibi_slopes", ctypes.c_void_p), ("partition_size", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("device_error", ctypes.c_void_p)]
+                ("device_error", ctypes.c_void_p), ("first_wait_limit", ctypes.c_int)]
 
 
 class PAError(RuntimeError):
@@ -200,13 +200,14 @@ def pa_reshape_and_cache_opt(key, value, k_cache, v_cache, slot_mapping, kv_dtyp
 
 def pa_decode_opt(out, q, k_cache, v_cache, block_table, seq_lens, scale: float, num_kv_heads: int,
                   k_scale=None, v_scale=None, scale_stride: int = 0, alibi_slopes=None, partition_size: int = 0,
-                  workspace=None, device_error=None, stream=None) -> None:
+                  workspace=None, device_error=None, stream=None, first_wait_limit: int = 0) -> None:
     """pa_decode with every option: per-head FP8 scales (KV head h uses k_scale[h * scale_stride]),
     ALiBi slopes (fp32 [Hq]: logit += slope_h * (t - (seq_len - 1))), partition size, caller
-    workspace (None: the library's internal one) and device error word."""
+    workspace (None: the library's internal one) and device error word.  first_wait_limit: poll
+    limit of the first pipeline wait (0 normal, < 0 give up at once), for testing the timeout path."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     o = PaDecodeOptions(_ptr(k_scale), _ptr(v_scale), int(scale_stride), _ptr(alibi_slopes), int(partition_size),
-                        _ptr(workspace), ws_bytes, _ptr(device_error))
+                        _ptr(workspace), ws_bytes, _ptr(device_error), int(first_wait_limit))
     args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(block_table), desc(seq_lens))
     rc = lib().pa_decode_opt(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads), ctypes.byref(o),
                              _stream(stream))
@@ -216,7 +217,7 @@ def pa_decode_opt(out, q, k_cache, v_cache, block_table, seq_lens, scale: float,
 def pa_decode_step(out, q, key, value, k_cache, v_cache, slot_mapping, block_table, seq_lens, scale: float,
                    num_kv_heads: int, new_rows_start=None, k_scale=None, v_scale=None, scale_stride: int = 0,
                    alibi_slopes=None, partition_size: int = 0, workspace=None, device_error=None,
-                   stream=None) -> None:
+                   stream=None, first_wait_limit: int = 0) -> None:
     """The cache write of the step's new rows (key / value [T, Hkv, D] to slot_mapping) and the
     decode over the updated cache in one call; the decode reads everything but the new
     positions while the write runs.  new_rows_start: None (row s = sequence s's newest token)
@@ -224,7 +225,7 @@ def pa_decode_step(out, q, key, value, k_cache, v_cache, slot_mapping, block_tab
     the scales also quantise the rows written to an FP8 cache."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     o = PaDecodeOptions(_ptr(k_scale), _ptr(v_scale), int(scale_stride), _ptr(alibi_slopes), int(partition_size),
-                        _ptr(workspace), ws_bytes, _ptr(device_error))
+                        _ptr(workspace), ws_bytes, _ptr(device_error), int(first_wait_limit))
     nrs = None if new_rows_start is None else ctypes.byref(desc(new_rows_start))
     args = (desc(out), desc(q), desc(key), desc(value), desc(k_cache), desc(v_cache), desc(slot_mapping))
     rc = lib().pa_decode_step(*[ctypes.byref(a) for a in args], nrs, ctypes.byref(desc(block_table)),
@@ -236,14 +237,14 @@ def pa_decode_step(out, q, key, value, k_cache, v_cache, slot_mapping, block_tab
 def pa_attention_varlen(out, q, k_cache, v_cache, query_start_loc, block_table, seq_lens, scale: float,
                         num_kv_heads: int, max_query_len: int, k_scale=None, v_scale=None, scale_stride: int = 0,
                         alibi_slopes=None, partition_size: int = 0, workspace=None, device_error=None,
-                        stream=None) -> None:
+                        stream=None, first_wait_limit: int = 0) -> None:
     """Several new query tokens per sequence: q/out [Tq, Hq, D] packed, sequence s owning rows
     query_start_loc[s] .. query_start_loc[s+1]-1 (int32 [S+1]); query i of s sits at position
     seq_lens[s] - n_s + i and sees the tokens up to it.  Options as pa_decode_opt; the workspace
     size is pa_decode_workspace_size with num_heads = Hq * max_query_len."""
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     o = PaDecodeOptions(_ptr(k_scale), _ptr(v_scale), int(scale_stride), _ptr(alibi_slopes), int(partition_size),
-                        _ptr(workspace), ws_bytes, _ptr(device_error))
+                        _ptr(workspace), ws_bytes, _ptr(device_error), int(first_wait_limit))
     args = (desc(out), desc(q), desc(k_cache), desc(v_cache), desc(query_start_loc), desc(block_table),
             desc(seq_lens))
     rc = lib().pa_attention_varlen(*[ctypes.byref(a) for a in args], float(scale), int(num_kv_heads),

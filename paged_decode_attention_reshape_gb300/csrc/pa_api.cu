@@ -463,7 +463,8 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
                 const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
                 const pa_decode_options &o, bool internal_ws, pa_stream_t stream,
                 const pa_tensor *query_start_loc = nullptr, int max_query_len = 1,
-                const pa_tensor *new_rows_start = nullptr, bool early = false, bool dry = false) {
+                const pa_tensor *new_rows_start = nullptr, bool early = false, bool dry = false,
+                size_t *ws_need = nullptr, size_t *ws_counters = nullptr) {
   const float *k_scale = o.k_scale, *v_scale = o.v_scale;
   const int partition_size = o.partition_size;
   void *workspace = o.workspace;
@@ -563,6 +564,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   p.max_parts = max_parts;
   p.cluster = pl.cluster;
   p.flat = pl.flat;
+  p.first_wait_limit = o.first_wait_limit;
   p.early = early && !varlen ? 1 : 0;
   p.new_start = p.early && new_rows_start ? static_cast<const int32_t *>(new_rows_start->data) : nullptr;
   p.err = device_error;
@@ -579,10 +581,14 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   if (static_cast<int64_t>(p.Hkv) * p.HG > 65535) return PA_ERR_UNSUPPORTED_SHAPE;
 
   if (dry) {  // validation only (pa_decode_step checks everything before its first launch)
-    if (((max_parts > 1 && pl.cluster <= 1) || pl.flat > 0) && !internal_ws) {
+    if ((max_parts > 1 && pl.cluster <= 1) || pl.flat > 0) {
       const WsLayout lay = workspace_layout(S, Hqv, Hkv, D, maxNB, P, pl.flat);
-      if (!workspace || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
-      if (!aligned16(workspace)) return PA_ERR_ALIGNMENT;
+      if (ws_need) *ws_need = lay.total;
+      if (ws_counters) *ws_counters = lay.ml_off;
+      if (!internal_ws) {
+        if (!workspace || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return PA_ERR_ALIGNMENT;
+      }
     }
     return PA_OK;
   }
@@ -638,6 +644,22 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
 }
 
 }  // namespace
+
+int pa::decode_ex_requirements(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                           const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                           const float *k_scale, const float *v_scale, int partition_size, int *device_error,
+                           size_t *ws_bytes, size_t *counter_bytes) {
+  pa_decode_options o{};
+  o.k_scale = k_scale;
+  o.v_scale = v_scale;
+  o.partition_size = partition_size;
+  o.device_error = device_error;
+  *ws_bytes = 0;
+  *counter_bytes = 0;
+  // internal_ws: the workspace is not checked here (the caller supplies it afterwards)
+  return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, true, nullptr,
+                     nullptr, 1, nullptr, false, true, ws_bytes, counter_bytes);
+}
 
 PA_API int pa_decode_ex(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
                         const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,

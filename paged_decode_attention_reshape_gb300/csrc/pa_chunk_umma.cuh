@@ -190,8 +190,9 @@ struct UmmaCfg {
 };
 
 // Bounded mbarrier wait that also gives up once another role has set *abort.
-__device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-  for (uint32_t i = 0; i < kUmmaWaitLimit; ++i) {
+__device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint32_t limit = kUmmaWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
   }
@@ -296,13 +297,13 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   const uint32_t tl = tmem + 256u * tile + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
   float l = 0.f;
   bool ok = true;
+  int issued = 0;  // TMA producer: K/V groups issued
 
   if (warp == C::TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
     const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
     const uint64_t pol = policy_evict_normal();  // the other row tiles of (s, g) read the same pages
     const int c1 = p.nhd ? g : 0, c2 = p.nhd ? 0 : g;
-    int issued = 0;
     for (int k = 0; k < ngr; ++k) {
       const int gs = k % C::NS;
       if (k >= C::NS && !__all_sync(0xffffffffu, umma_wait(empty0 + 8 * gs, ((k / C::NS) - 1) & 1, abort))) break;
@@ -328,12 +329,6 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       }
       issued = k + 1;
     }
-    if (*abort && lane == 0) {
-      // loads may still be in flight into the ring: wait (bounded) for the latest group of
-      // every slot before the CTA's shared memory goes away
-      for (int k2 = max(0, issued - C::NS); k2 < issued; ++k2)
-        mbar_wait_bounded(full0 + 8 * (k2 % C::NS), (k2 / C::NS) & 1, kUmmaWaitLimit);
-    }
   } else if (warp >= C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer of tile t
     // The whole warp runs the loop, so descriptors and addresses are warp-uniform values;
@@ -352,7 +347,11 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       for (int k = 0; k <= ngr; ++k) {
         if (k < ngr) {
           const int gs = k % C::NS;
-          if (!__all_sync(0xffffffffu, umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort))) break;
+          // the first group's wait may carry a shorter limit (first_wait_limit: the abort path's test)
+          const uint32_t lim = (k == 0 && p.first_wait_limit != 0)
+                                   ? (p.first_wait_limit < 0 ? 0u : static_cast<uint32_t>(p.first_wait_limit))
+                                   : kUmmaWaitLimit;
+          if (!__all_sync(0xffffffffu, umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort, lim))) break;
           umma::fence_after();
           const uint64_t kd = kd0 + ((gs * C::GP * C::BOXB) >> 4);
           if (elect_one()) {
@@ -388,11 +387,6 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
           }
           __syncwarp();
         }
-      }
-      if (*abort) {
-        if (elect_one()) umma::commit(drain(t));  // every MMA of this issuer has completed once this arrives
-        __syncwarp();
-        mbar_wait_bounded(drain(t), 0, kUmmaWaitLimit);
       }
     }
   } else if (tile < ntiles) {
@@ -518,6 +512,22 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   // every role has left its loop (a block-table error it found is visible from here on)
   umma::fence_before();
   __syncthreads();
+  if (*abort) {
+    // A role gave up (final from here on: every role has left its loop).  Copies and MMAs may
+    // still be in flight: the producer waits (bounded) for the latest group of every ring slot,
+    // each MMA issuer for the completion of every MMA it issued, before the shared memory and
+    // the tensor memory are released.
+    if (warp == C::TMA_WARP) {
+      if (lane == 0)
+        for (int k2 = max(0, issued - C::NS); k2 < issued; ++k2)
+          mbar_wait_bounded(full0 + 8 * (k2 % C::NS), (k2 / C::NS) & 1, kUmmaWaitLimit);
+    } else if (warp >= C::MMA_WARP && warp - C::MMA_WARP < ntiles) {
+      const int t = warp - C::MMA_WARP;
+      if (elect_one()) umma::commit(drain(t));  // arrives once every MMA of this issuer has completed
+      __syncwarp();
+      mbar_wait_bounded(drain(t), 0, kUmmaWaitLimit);
+    }
+  }
   if (warp < 4 * T && tile < ntiles) {
     // ---- epilogue: O / l -> out
     if (ok && __all_sync(0xffffffffu, umma_wait(odone(tile), (ngr - 1) & 1, abort))) {

@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(W * 32) decode_f32_kernel(const DecodeParams p
   }
   static_assert(sizeof(sm) >= 8 * kMergeSmemParts * 4, "merge weights reuse sm");
   if (!direct)
-    merge_if_last<float, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, ng, nparts, 1.f, W * 32,
-                            &sm[0][0][0], rows);
+    merge_if_last<float, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, ng, nparts, 1.f, any_bad,
+                            W * 32, &sm[0][0][0], rows);
 }
 
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st) {

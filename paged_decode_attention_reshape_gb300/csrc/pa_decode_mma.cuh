@@ -241,11 +241,18 @@ __device__ __forceinline__ bool run_pages(const DecodeParams &p, const CUtensorM
   for (int k = 0; k < nmine; ++k) {
     const int u = u0 + k;  // this page's use of the warp's stages
     const int st = u % STAGES;
-    if (!mbar_wait_bounded(bar0 + 8 * st, (u / STAGES) & 1, kWaitLimit)) {
+    // the warp's first wait may carry a shorter limit (first_wait_limit: the timeout path's test)
+    const uint32_t lim = (u == 0 && p.first_wait_limit != 0)
+                             ? (p.first_wait_limit < 0 ? 0u : static_cast<uint32_t>(p.first_wait_limit))
+                             : kWaitLimit;
+    if (!mbar_wait_bounded(bar0 + 8 * st, (u / STAGES) & 1, lim)) {
       bad = true;
       stalled = true;
       if (lane == 0 && p.err) atomicOr(p.err, kErrTimeout);
-      for (int k2 = k + 1; k2 < min(nmine, k + STAGES); ++k2)  // drain copies in flight
+      // Drain: the copies of pages k .. k+STAGES-1 (the one just given up on included) are in
+      // flight; wait for every one of them, with the full limit, before the warp reuses its
+      // stage region for its merge state or the CTA exits.
+      for (int k2 = k; k2 < min(nmine, k + STAGES); ++k2)
         mbar_wait_bounded(bar0 + 8 * ((u0 + k2) % STAGES), ((u0 + k2) / STAGES) & 1, kWaitLimit);
       break;
     }
@@ -657,7 +664,7 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
         // a CTA with an error still counts itself, so the unit's counter returns to zero
         const int c0 = owner(ps);
         merge_if_last<OutT, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * z, ng, owner(pn - 1) - c0 + 1,
-                               vs, C::THREADS, smem_w,
+                               vs, any_bad, C::THREADS, smem_w,
                                FlatRows{static_cast<int64_t>(blockIdx.y) * p.flat + c0, range_start(c0) < ps ? 1 : 0});
       }
       x = y;
@@ -770,10 +777,11 @@ __global__ void __launch_bounds__(W * 32, mma_min_ctas(KIND, D))
   const FixedRows rows{(static_cast<int64_t>(s) * p.Hkv + g) * p.VH + v0, p.max_parts};
   if (!any_bad)
     write_cta_state<KIND, D, W, STAGES, OutT>(p, sgen, cm, ng, vs, direct, [&](int hh) { return rows(hh, part); });
-  // a CTA with an error still counts itself, so the unit's counter returns to zero
+  // a CTA with an error still counts itself (so the unit's counter returns to zero) and marks
+  // the unit, whose merge then writes nothing
   if (!direct)
-    merge_if_last<OutT, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, ng, nparts, vs, C::THREADS,
-                           smem_w, rows);
+    merge_if_last<OutT, D>(p, cm, static_cast<int>(blockIdx.y) + p.Hkv * p.HG * s, ng, nparts, vs, any_bad,
+                           C::THREADS, smem_w, rows);
 }
 
 // Host side of one (kind, head size) instantiation: function attributes, launch and

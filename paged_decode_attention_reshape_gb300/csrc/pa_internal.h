@@ -74,6 +74,10 @@ struct DecodeParams {
   int early;
   const int32_t *new_start;
   int flat;                            // > 0: balanced split, this many CTAs per head row (S <= kFlatMaxSeqs)
+  // Poll limit of the first pipeline wait (decode: each warp's first page; query tile: the
+  // first K/V group): 0 = the normal limit, > 0 = that many polls, < 0 = give up at once.
+  // Tests use it to make a bounded wait run out; every later wait and drain keeps the normal limit.
+  int first_wait_limit;
   // fp32 path only: direct cache pointers and strides (elements)
   const float *kc, *vc;
   int64_t kc_s0, kc_s1, kc_s2, vc_s0, vc_s1, vc_s2;
@@ -100,6 +104,15 @@ constexpr int kErrSlot = PA_DEVERR_SLOT_RANGE;
 constexpr int kErrBlock = PA_DEVERR_BLOCK_RANGE;
 constexpr int kErrSeqLen = PA_DEVERR_SEQLEN_RANGE;
 constexpr int kErrTimeout = PA_DEVERR_WAIT_TIMEOUT;
+
+// Every check pa_decode_ex makes, without launching or allocating anything; on PA_OK,
+// *ws_bytes is the split-KV workspace the call will need and *counter_bytes the size of the
+// arrival-counter region at its start, which must be zero when the decode starts (both 0
+// when the call does not split or uses the cluster split).  Used by pa_decode_noalloc.
+int decode_ex_requirements(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, const pa_tensor *v_cache,
+                           const pa_tensor *block_table, const pa_tensor *seq_lens, float scale, int num_kv_heads,
+                           const float *k_scale, const float *v_scale, int partition_size, int *device_error,
+                           size_t *ws_bytes, size_t *counter_bytes);
 
 // Launchers (defined next to their kernels).  Return a cudaError_t.
 cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, int sm_count, cudaStream_t st);

@@ -44,22 +44,31 @@ struct FlatRows {
   }
 };
 
+// A part that stored no state (a bad block id or a timed-out wait: `bad`) still arrives, so
+// the counter returns to zero, but first sets kUnitBad in it; the last arriver then sees the
+// flag and writes nothing for the unit (its error bit is already set).  Each thread's
+// operations on one location are ordered, so a bad part's flag precedes its own arrival,
+// and the last arrival follows every other.
+constexpr int kUnitBad = 0x40000000;
+constexpr int kArrivalMask = kUnitBad - 1;
+
 // smem_w: shared memory for 8 * kMergeSmemParts floats, free for reuse by now.
 // rows(hh, i): workspace row of column hh in the unit's i-th part; cm maps columns to outputs.
 template <typename OutT, int D, typename Rows>
 __device__ __forceinline__ void merge_if_last(const DecodeParams &p, const Cols &cm, int unit, int ng, int nparts,
-                                              float vs, int threads, float *smem_w, Rows rows) {
+                                              float vs, bool bad, int threads, float *smem_w, Rows rows) {
   __shared__ int s_last;
   float(*s_w)[kMergeSmemParts] = reinterpret_cast<float(*)[kMergeSmemParts]>(smem_w);  // weight per head, part
   __syncthreads();  // every partial store of this CTA precedes thread 0's release below
   if (threadIdx.x == 0) {
+    if (bad) atomicOr(p.counters + unit, kUnitBad);
     int old;
     // release: this CTA's partial states become visible before the arrival counts;
     // acquire: the last arriver then sees every other partition's state
     asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + unit) : "memory");
-    const int last = old == nparts - 1;
+    const int last = (old & kArrivalMask) == nparts - 1;
     if (last) atomicExch(p.counters + unit, 0);
-    s_last = last;
+    s_last = last && !(old & kUnitBad) && !bad;
   }
   __syncthreads();
   if (!s_last) return;

@@ -19,7 +19,7 @@
 
 #include <mutex>
 
-#include "../../include/pa.h"
+#include "pa_internal.h"
 
 #define PA_API extern "C" __attribute__((visibility("default")))
 
@@ -51,33 +51,25 @@ PA_API int pa_decode_noalloc(pa_tensor *out, const pa_tensor *q, const pa_tensor
                              const pa_tensor *v_cache, const pa_tensor *block_table, const pa_tensor *seq_lens,
                              float scale, int num_kv_heads, const float *k_scale, const float *v_scale,
                              int partition_size, int *device_error, pa_stream_t stream) {
-  if (!q || !k_cache || !block_table || q->ndim != 3 || k_cache->ndim != 4 || block_table->ndim != 2)
-    return PA_ERR_INVALID_ARG;
-  const int S = static_cast<int>(q->shape[0]), Hq = static_cast<int>(q->shape[1]);
-  const int D = static_cast<int>(q->shape[2]), max_blocks = static_cast<int>(block_table->shape[1]);
-  if (num_kv_heads <= 0 || Hq <= 0 || Hq % num_kv_heads) return PA_ERR_INVALID_ARG;
-
-  // How much scratch this call needs: none when the plan does not split.
-  int P = 0, nparts = 1;
-  int rc = pa_decode_plan(S, Hq, num_kv_heads, D, max_blocks, k_cache->dtype, 0, partition_size, &P, &nparts);
+  // Every argument is checked first, exactly as pa_decode_ex checks it, and the scratch the
+  // call's own plan needs is computed; nothing is launched before that.
+  size_t need = 0, counter_bytes = 0;
+  int rc = pa::decode_ex_requirements(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, k_scale,
+                                      v_scale, partition_size, device_error, &need, &counter_bytes);
   if (rc != PA_OK) return rc;
-  const size_t need = (P > 0 || P == PA_PARTITION_BALANCED)
-                          ? pa_decode_workspace_size(S, Hq, num_kv_heads, D, max_blocks, P)
-                          : 0;
   if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;  // bigger than the fixed buffer
 
   void *scratch = nullptr;
-  if (need > 0) {
-    if ((rc = scratch_address(&scratch)) != PA_OK) return rc;
-    // The split-KV arrival counters sit at the start of the scratch and must be
-    // zero when the decode starts.  The previous call may have left partial
-    // results there (a different shape puts them at different offsets), so the
-    // counter region is cleared on the call's stream first.
-    const int G = Hq / num_kv_heads;
-    const size_t counter_bytes = static_cast<size_t>(S) * num_kv_heads * ((G + 7) / 8) * sizeof(int);
+  if ((rc = scratch_address(&scratch)) != PA_OK) return rc;
+  if (counter_bytes > 0) {
+    // The split-KV arrival counters sit at the start of the scratch and must be zero when
+    // the decode starts.  The previous call may have left partial results there (a
+    // different shape puts them at different offsets), so the counter region is cleared
+    // on the call's stream first.
     if (cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return PA_ERR_CUDA;
   }
+  // The whole buffer is always passed, so pa_decode_ex never takes an allocating path.
   return pa_decode_ex(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, k_scale, v_scale,
-                      partition_size, scratch, need > 0 ? PA_NOALLOC_SCRATCH_BYTES : 0, device_error, stream);
+                      partition_size, scratch, PA_NOALLOC_SCRATCH_BYTES, device_error, stream);
 }
