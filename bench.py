@@ -2,24 +2,27 @@
 """Benchmark of the paged KV-cache hot path on GB300.
 
 One step = one pass of the whole path over one batch: the cache write of the
-step's new tokens (pa_reshape_and_cache) followed by paged decode attention
-(pa_decode_ex: decode kernel, plus the split-KV reduce when the plan splits).
+step's new tokens followed by paged decode attention (pa_decode_step: the write,
+then the decode kernel with its fused split-KV merge when the plan splits).
 
-Default workload: the small GQA bf16 decode (64 sequences, 32 query / 8 KV
-heads, head size 64, lengths uniform in [1, 2048], 2 GiB pool of 65536 blocks,
-64 new tokens written per step).  ``--config c3|c4|c5`` measures the other
-configurations.  L2 is flushed (a 512 MiB write) before every timed step,
-outside the timed events.
+Headline workload (``--config``, default c3): the 8B-class batched decode (256
+sequences, 32 query / 8 KV heads, head size 128, bf16, lengths uniform in
+[512, 4096], 256 new tokens written per step) -- the largest configuration.  The
+same line carries, under ``configs``, the same measurement of the other
+workloads (c2 small GQA decode, c4 long-context split-KV decode, c5 FP8 write +
+decode, c3-chunk128 chunked prefill on the query-tile kernel).  L2 is flushed (a
+512 MiB write and a 512 MiB read) before every timed step, outside the events.
 
-Prints one JSON line.  ``value`` = paged-decode KV-read GB/s over the whole step
-(algorithmic decode bytes / step time; the step -- the same library calls -- is
-captured once in a CUDA graph and replayed, as a serving loop replays its decode
-step; ``eager_ms_per_step`` times the calls issued one by one from Python);
-``roofline`` is for the decode kernel
-alone (profiling events on its launch stream); ``e2e`` repeats the step from
-pinned host buffers with the host<->device copies inside the timed region;
+Per workload: ``value`` = paged-decode KV-read GB/s over the whole step
+(algorithmic decode bytes / step time; the step is captured once in a CUDA graph
+and replayed, as a serving loop replays its decode step; ``eager_ms_per_step``
+times the calls issued one by one from Python); ``roofline`` is for the attention
+kernel alone (profiling events on its launch stream); ``e2e`` repeats the step
+from pinned host buffers with the host<->device copies inside the timed region;
 ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same
-workload.  ``--impl reference`` times that oracle as the reference arm.
+workload.  ``--impl reference`` times that oracle as the reference arm;
+``--sweep-partitions`` times the decode kernel over the partition sizes the
+library's partition plan is fitted to.
 """
 from __future__ import annotations
 
@@ -572,81 +575,59 @@ def _workload_desc(w):
                w.num_blocks, w.T))
 
 
-def main(argv=None):
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="c2", choices=sorted(configs.BUILDERS))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--partition-size", type=int, default=0)
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--quick", action="store_true", help="setup + warm-up steps only (profiling runs)")
-    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the timed steps")
-    args = ap.parse_args(argv)
-    if args.impl == "reference":
-        return main_reference(args)
-    if args.warmup < 3:
-        args.warmup = 3
+# The workloads measured beside the headline one, each in the same JSON line: every decode
+# workload of the configurations plus the chunked-prefill step on the query-tile kernel.
+EXTRA_CONFIGS = ("c2", "c4", "c5", "c3-chunk128")
 
+
+def measure(w, args, flush, sampler, ws=1, rank=0, cpu_target_s=12.0, partition_size=None, steps=None,
+            e2e=True, soak_s=1.0):
+    """Stage workload `w`, time K steps of the hot path on it and return its JSON fields.
+    The step is captured in a CUDA graph and replayed K times (L2 flushed before each, outside
+    the events); the same steps launched call by call, replayed warm (no flush), and a pass with
+    the library's per-kernel profiling events give the other timings."""
     import paged_decode_attention_reshape_gb300 as pa
-    pa.lib()
-    ws, rank, local = dist_setup()
     dev = "cuda"
-    w = configs.get(args.config)
+    K = args.steps if steps is None else steps
+    part = args.partition_size if partition_size is None else partition_size
     st = stage(w, dev)
-    P, nparts, wspace = workspace_for(st, args.partition_size)
-    flush = L2Flush(dev)
+    P, nparts, wspace = workspace_for(st, part)
     for _ in range(args.warmup):
         flush()
-        run_step(st, args.partition_size, wspace)
+        run_step(st, part, wspace)
     torch.cuda.synchronize()
-    if args.quick:
-        rc, bits = pa.pa_check_device_error(st.err)
-        if rc != 0:
-            raise SystemExit("device error %d bits %d" % (rc, bits))
-        print(json.dumps({"quick": True, "config": w.name, "partition": P}), flush=True)
-        return 0
-
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    if sampler:
-        sampler.start()
-        time.sleep(0.5)
-        # soak: keep the GPU busy ~1 s so the sampled clocks are the loaded ones
-        t_end = time.time() + (0.0 if args.no_soak else 1.0)
+    if sampler and soak_s > 0:
+        # soak: keep the GPU busy so the sampled clocks are the loaded ones
+        t_end = time.time() + soak_s
         while time.time() < t_end:
             for _ in range(20):
                 flush()
-                run_step(st, args.partition_size, wspace)
+                run_step(st, part, wspace)
             torch.cuda.synchronize()
-    graph = capture_step(st, args.partition_size, wspace)
+    graph = capture_step(st, part, wspace)
     for _ in range(3):
         flush()
         graph.replay()
     barrier(ws)
     torch.cuda.synchronize()
     t0 = time.time()
-    step_ms, _ = time_steps(st, args.steps, flush, args.partition_size, wspace, profile=False, graph=graph)
+    step_ms, _ = time_steps(st, K, flush, part, wspace, profile=False, graph=graph)
     t1 = time.time()
     barrier(ws)
     # the same steps launched one call at a time from Python (reported beside the graph time)
-    eager_ms, _ = time_steps(st, args.steps, flush, args.partition_size, wspace, profile=False)
+    eager_ms, _ = time_steps(st, K, flush, part, wspace, profile=False)
     # and replayed back to back without the L2 flush (warm: what the previous step left in L2)
-    warm_ms, _ = time_steps(st, args.steps, lambda: None, args.partition_size, wspace, profile=False, graph=graph)
+    warm_ms, _ = time_steps(st, K, lambda: None, part, wspace, profile=False, graph=graph)
     # per-kernel device times: the same steps again with the library's profiling events
     # around each launch (kept out of the step timing above: an event between the write and
     # the decode would hold back the decode's programmatic early launch)
-    _, prof = time_steps(st, args.steps, flush, args.partition_size, wspace, profile=True)
+    _, prof = time_steps(st, K, flush, part, wspace, profile=True)
     clocks = sampler.summary(t0 - 0.15, t1 + 0.15) if sampler else None
-    if sampler:
-        sampler.stop()
     rc, bits = pa.pa_check_device_error(st.err)
     if rc != 0:
-        raise SystemExit("device error word set: status %d bits %d" % (rc, bits))
+        raise SystemExit("%s: device error word set: status %d bits %d" % (w.name, rc, bits))
 
-    ms = float(np.mean(step_ms))
-    ms = max_over_ranks(ms, ws)
+    ms = max_over_ranks(float(np.mean(step_ms)), ws)
     eager = max_over_ranks(float(np.mean(eager_ms)), ws)
     warm = max_over_ranks(float(np.mean(warm_ms)), ws)
     pct = [float(x) for x in np.percentile(step_ms, [10, 50, 90])]
@@ -657,8 +638,7 @@ def main(argv=None):
     dk_avg = dk_ms / max(1, dk_n)
     peak, peak_src = _peaks()
     achieved = dec_bytes / (dk_avg * 1e-3) / 1e9
-    launches = wr_n + dk_n
-    if w.query_tile() and args.partition_size in (0, -1):
+    if w.query_tile() and part in (0, -1):
         # tensor-bound: algorithmic FLOPs against the sustained bf16 peak (the kernel runs
         # inside a seconds-long loop of steps)
         flops = w.attention_flops()
@@ -667,47 +647,171 @@ def main(argv=None):
         roofline = {"bound": "tensor", "achieved": tach, "peak": tpeak, "unit": "TFLOP/s", "frac": tach / tpeak,
                     "traffic": _ncu_traffic(w.name, CHUNK_SOURCES), "peak_source": tsrc + " (sustained)",
                     "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": dec_bytes,
-                    "hbm_GB/s": achieved, "kernel": "chunk_umma_kernel"}
+                    "hbm_GB/s": achieved, "kernel": "chunk_umma_kernel", "kernel_us": dk_avg * 1e3}
     else:
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": _ncu_traffic(w.name), "peak_source": peak_src,
-                    "algorithmic_bytes_per_launch": dec_bytes, "kernel": "decode_mma_kernel"}
+                    "algorithmic_bytes_per_launch": dec_bytes, "kernel": "decode_mma_kernel",
+                    "kernel_us": dk_avg * 1e3}
 
-    e2e = None
-    if not args.no_e2e:
-        e_ms, h2d, d2h = e2e_steps(st, max(10, min(args.steps, 200)), flush, args.partition_size, wspace)
+    e2e_d = None
+    if e2e:
+        e_ms, h2d, d2h = e2e_steps(st, max(10, min(K, 200)), flush, part, wspace)
         em = max_over_ranks(float(np.mean(e_ms)), ws)
-        e2e = {"value": job_throughput(dec_bytes, ws, em), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": em}
+        e2e_d = {"value": job_throughput(dec_bytes, ws, em), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "ms_per_step": em}
+    del graph, st, wspace
+    torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+    if rank == 0 and cpu_target_s > 0:
+        cpu = cpu_baseline(w, target_s=cpu_target_s)
         if w.S <= 64 and w.nq == 1:   # the small decode workloads: one host thread as well
-            cpu["single_thread"] = cpu_baseline(w, target_s=4.0, threads=1)
+            cpu["single_thread"] = cpu_baseline(w, target_s=min(4.0, cpu_target_s), threads=1)
 
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.cache_dtype if w.cache_dtype != "auto" else w.dtype,
-        "data": "synthetic",
-        "config": {"workload": w.name + " " + _workload_desc(w), "l2": "flushed before each step (512 MiB write + 512 MiB read)",
-                   "partition_tokens": P, "partitions_max": nparts, "parallelism": "replicas" if ws > 1 else "1 GPU"},
+    return {
+        "value": value, "unit": "GB/s", "ms_per_step": ms, "steps": K,
+        "config": {"workload": w.name + " " + _workload_desc(w),
+                   "l2": "flushed before each step (512 MiB write + 512 MiB read)",
+                   "partition_tokens": P, "partitions_max": nparts,
+                   "parallelism": "replicas" if ws > 1 else "1 GPU"},
+        "dtype": w.cache_dtype if w.cache_dtype != "auto" else w.dtype,
         "pct_of_hbm_peak": 100.0 * value / peak,
         "tokens_per_s": ws * w.S * w.nq / (ms * 1e-3),
         "step_ms_p10_p50_p90": pct,
-        "launch": "step replayed from a CUDA graph (write + attention, programmatic-launch edge kept)",
         "eager_ms_per_step": eager, "eager_value": job_throughput(dec_bytes, ws, eager),
         "warm_ms_per_step": warm, "warm_value": job_throughput(dec_bytes, ws, warm),
         "decode_kernel_us": dk_avg * 1e3,
         "cache_write": {"GB/s": w.write_bytes() / ((wr_ms / max(1, wr_n)) * 1e-3) / 1e9,
                         "kernel_us": wr_ms / max(1, wr_n) * 1e3, "bytes": w.write_bytes()},
         "roofline": roofline,
-        "gpu_launches": launches,
+        "gpu_launches": wr_n + dk_n,
         "clocks": clocks,
-        "e2e": e2e,
+        "e2e": e2e_d,
         "cpu_baseline": cpu,
     }
+
+
+# Partition sizes of the sweep (tokens; 0 = the library's plan, -1 = never split, -2 = the
+# two-CTA cluster split, PA_PARTITION_BALANCED = the balanced split).
+SWEEP = {"c4": [128, 256, 512, 1024, 2048, 4096, 8192, -2, -100, 0, -1],
+         "c2": [256, 512, 1024, -2, -100, 0, -1],
+         "c3": [512, 1024, 2048, -100, 0, -1],
+         "c5": [512, 1024, 2048, -100, 0, -1]}
+
+
+def sweep_partitions(args, flush):
+    """Decode-kernel time of each workload at each partition size of SWEEP: the measurements
+    the partition plan is fitted to.  Prints one JSON line per point and a Markdown table."""
+    import paged_decode_attention_reshape_gb300 as pa
+    names = args.sweep_configs.split(",") if args.sweep_configs else list(SWEEP)
+    rows = []
+    for name in names:
+        w = configs.get(name)
+        st = stage(w, "cuda")
+        for part in SWEEP[name]:
+            P, nparts, wspace = workspace_for(st, part)
+            for _ in range(args.warmup):
+                flush()
+                run_step(st, part, wspace)
+            _, prof = time_steps(st, args.steps, flush, part, wspace, profile=True)
+            rc, bits = pa.pa_check_device_error(st.err)
+            if rc != 0:
+                raise SystemExit("%s P=%d: device error %d bits %d" % (name, part, rc, bits))
+            dk_ms, dk_n = prof[pa.PA_KERNEL_DECODE]
+            us = dk_ms / max(1, dk_n) * 1e3
+            gbs = w.decode_bytes() / (us * 1e-6) / 1e9
+            r = {"sweep": name, "request": part, "partition_tokens": P, "partitions_max": nparts,
+                 "decode_kernel_us": us, "GB/s": gbs, "frac": gbs / _peaks()[0], "steps": dk_n}
+            rows.append(r)
+            print(json.dumps(r), flush=True)
+            del wspace
+        del st
+        torch.cuda.empty_cache()
+    label = {0: "plan", -1: "unsplit", -2: "cluster x2", -100: "balanced"}
+    print("| workload | request | partition (tokens) | partitions | decode kernel (us) | GB/s | frac of measured peak |")
+    print("|---|---|---|---|---|---|---|")
+    for r in rows:
+        req = label.get(r["request"], str(r["request"]))
+        pt = {0: "unsplit", -100: "balanced"}.get(r["partition_tokens"], str(r["partition_tokens"]))
+        print("| %s | %s | %s | %d | %.1f | %.0f | %.3f |" % (r["sweep"], req, pt, r["partitions_max"],
+                                                            r["decode_kernel_us"], r["GB/s"], r["frac"]))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="c3", choices=sorted(configs.BUILDERS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--extra-configs", default=",".join(EXTRA_CONFIGS),
+                    help="workloads measured beside the headline one, in the same line ('' for none)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="setup + warm-up steps only (profiling runs)")
+    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the timed steps")
+    ap.add_argument("--sweep-partitions", action="store_true",
+                    help="time the decode kernel over the partition sizes the plan is fitted to")
+    ap.add_argument("--sweep-configs", default="", help="workloads of the sweep (default: all)")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return main_reference(args)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import paged_decode_attention_reshape_gb300 as pa
+    pa.lib()
+    ws, rank, local = dist_setup()
+    flush = L2Flush("cuda")
+    if args.sweep_partitions:
+        return sweep_partitions(args, flush)
+    w = configs.get(args.config)
+    if args.quick:
+        st = stage(w, "cuda")
+        P, nparts, wspace = workspace_for(st, args.partition_size)
+        for _ in range(args.warmup):
+            flush()
+            run_step(st, args.partition_size, wspace)
+        torch.cuda.synchronize()
+        rc, bits = pa.pa_check_device_error(st.err)
+        if rc != 0:
+            raise SystemExit("device error %d bits %d" % (rc, bits))
+        print(json.dumps({"quick": True, "config": w.name, "partition": P}), flush=True)
+        return 0
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    soak = 0.0 if args.no_soak else 1.0
+    main_m = measure(w, args, flush, sampler, ws, rank, cpu_target_s=0 if args.no_cpu_baseline else 12.0,
+                     e2e=not args.no_e2e, soak_s=soak)
+    extras = {}
+    for name in [n for n in args.extra_configs.split(",") if n and n != args.config]:
+        # the other workloads: the same measurement, the default partition plan, a shorter
+        # CPU-oracle sample
+        extras[name] = measure(configs.get(name), args, flush, sampler, ws, rank,
+                               cpu_target_s=0 if args.no_cpu_baseline else 4.0, partition_size=0,
+                               e2e=not args.no_e2e, soak_s=min(soak, 0.3))
+    if sampler:
+        sampler.stop()
+
+    line = {
+        "metric": METRIC, "value": main_m["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main_m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": main_m["dtype"], "data": "synthetic",
+        "config": main_m["config"],
+        "launch": "step replayed from a CUDA graph (write + attention, programmatic-launch edge kept)",
+    }
+    for k in ("pct_of_hbm_peak", "tokens_per_s", "step_ms_p10_p50_p90", "eager_ms_per_step", "eager_value",
+              "warm_ms_per_step", "warm_value", "decode_kernel_us", "cache_write", "roofline", "gpu_launches",
+              "clocks", "e2e", "cpu_baseline"):
+        line[k] = main_m[k]
+    if extras:
+        line["configs"] = extras
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
