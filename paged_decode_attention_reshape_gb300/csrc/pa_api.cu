@@ -385,6 +385,17 @@ PA_API int pa_reshape_and_cache_opt(const pa_tensor *key, const pa_tensor *value
   p.v_scale = kv_dtype == PA_KV_FP8_E4M3 ? o.v_scale : nullptr;
   p.scale_stride = o.scale_stride;
   p.err = o.device_error;
+  {
+    // 32-bit index arithmetic when every byte offset the kernel forms stays below 2^31: the
+    // source rows (first to last element), the cache's block and token strides and the
+    // extent of one block (the block offset itself is one widening multiply)
+    const int64_t lim = INT32_MAX;
+    const int cb = elem_bytes(k_cache->dtype);
+    auto span = [&](const pa_tensor *t) { return ((T - 1) * t->stride[0] + (Hkv - 1) * t->stride[1] + D) * ib; };
+    auto inner = [&](const pa_tensor *c) { return ((Hkv - 1) * c->stride[1] + (kBlock - 1) * c->stride[2] + D) * cb; };
+    p.i32 = T <= lim && span(key) <= lim && span(value) <= lim && k_cache->stride[0] * cb <= lim &&
+            v_cache->stride[0] * cb <= lim && inner(k_cache) <= lim && inner(v_cache) <= lim;
+  }
   const int sm = device_sm_count();
   if (sm <= 0) return PA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

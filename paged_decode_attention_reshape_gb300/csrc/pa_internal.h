@@ -35,6 +35,8 @@ struct WriteParams {
   const float *k_scale, *v_scale;                   // nullable
   int64_t scale_stride;                             // 0: per tensor; else KV head h uses [h * stride]
   int *err;                                         // nullable
+  int i32;                                          // every source offset, cache stride and offset
+                                                    // within a block below 2^31 bytes
 };
 
 struct DecodeParams {

@@ -104,6 +104,13 @@ __device__ __forceinline__ Divisor make_divisor(float s) {
   return d;
 }
 
+// min(|x|, 2^80), NaN for a NaN x.
+__device__ __forceinline__ float clamp_mag(float x) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(x)), "f"(0x1p80f));
+  return r;
+}
+
 // E4M3 code pair of two quotients (cvt ... satfinite: round-to-nearest-even with
 // saturation); low byte = a.
 __device__ __forceinline__ uint32_t e4m3_pair(float a, float b) {
@@ -111,11 +118,37 @@ __device__ __forceinline__ uint32_t e4m3_pair(float a, float b) {
 }
 
 // One 16-byte pack of inputs -> E4M3 codes of x / scale (correctly rounded quotient).
+// 16-bit inputs: the codes of |x| / |s| are computed with |x| clamped to 2^80 (a NaN stays
+// NaN), which keeps the fused steps exact for every input -- nothing overflows, and a |x|
+// small enough for the steps to lose exactness gives a quotient far below the smallest E4M3
+// value -- and the sign of x / s is put back on each code (round to nearest even and
+// saturation are symmetric in the sign).  Zero, infinite and NaN inputs then need no branch.
 template <int DT>
 __device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, const Divisor &dv) {
   constexpr int E = 16 / In<DT>::bytes;
   float x[E], q[E];
   unpack8<DT>(v, x);
+  if constexpr (E == 8) {
+    if (dv.fast) {
+      const Divisor da{fabsf(dv.s), fabsf(dv.y), true};
+#pragma unroll
+      for (int i = 0; i < E; i += 2) {
+        const float2 r = da.div2_fast(clamp_mag(x[i]), clamp_mag(x[i + 1]));
+        q[i] = r.x;
+        q[i + 1] = r.y;
+      }
+      // sign bits of elements 0..3 and 4..7 (bit 15 of each 16-bit input) into bit 7 of
+      // each code byte, flipped for a negative scale
+      const uint32_t neg = dv.s < 0.f ? 0x80808080u : 0u;
+      uint2 o;
+      o.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
+      o.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
+      o.x |= (__byte_perm(v.x, v.y, 0x7531) ^ neg) & 0x80808080u;
+      o.y |= (__byte_perm(v.z, v.w, 0x7531) ^ neg) & 0x80808080u;
+      *reinterpret_cast<uint2 *>(dst) = o;
+      return;
+    }
+  }
   bool fast = dv.fast;
 #pragma unroll
   for (int i = 0; i < E; ++i) fast &= Divisor::in_range(x[i]);
@@ -145,8 +178,11 @@ __device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, const Divis
 // 8192-row E4M3 chunk (ALU-bound) at 18.4 us; 4 turns needed 80 registers (3 CTAs per SM)
 // and slowed the chunk to 20.5 us.
 constexpr int kBatch = 2;
+// CTAs per SM of the grid: the resident ones (the launch bound), so that every CTA is in
+// flight from the start and streams its tokens through the software pipeline.
+constexpr int kWriteCtasPerSm = 4;
 
-template <int DT, bool FP8>
+template <int DT, bool FP8, bool I32>
 __global__ void __launch_bounds__(256, 4) write_kernel(const WriteParams p) {
   // the decode that usually follows waits for this grid's completion before its first
   // read (griddepcontrol.wait), so it may be scheduled now
@@ -180,37 +216,64 @@ __global__ void __launch_bounds__(256, 4) write_kernel(const WriteParams p) {
     const int64_t e = static_cast<int64_t>(j0 - hcur * ppr) * EPP;
     const char *ks = static_cast<const char *>(p.key) + (hcur * p.key_hs + e) * IB;
     const char *vs = static_cast<const char *>(p.value) + (hcur * p.val_hs + e) * IB;
-    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * rows + tl; t0 < p.T; t0 += kBatch * stride) {
-      int64_t slot[kBatch];
-      uint4 kv[kBatch], vv[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int64_t t = t0 + u * stride;
-        slot[u] = -1;
-        if (t < p.T) {
-          slot[u] = __ldg(p.slot_mapping + t);
-          kv[u] = ld_once(ks + t * p.key_ts * IB);
-          vv[u] = ld_once(vs + t * p.val_ts * IB);
-        }
+    // Software pipeline over the thread's tokens: the slot and both source packs of the next
+    // token are in flight while the current one is converted and stored.  (Padding rows are
+    // loaded too; their sources are in bounds and nothing is written for them.)
+    // byte offsets: within a block and between tokens they fit 32 bits (I32); a block's
+    // offset is one widening multiply
+    const int64_t kin = (hcur * p.kc_s1 + e) * CB, vin = (hcur * p.vc_s1 + e) * CB;
+    auto process = [&](int64_t slot, const uint4 &kv, const uint4 &vv) {
+      if (slot < 0) return;  // padding row (or past the end): no destination
+      if (slot >= p.num_slots) {
+        if (p.err && j0 == 0) atomicOr(p.err, kErrSlot);
+        return;
       }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (slot[u] < 0) continue;  // padding row (or past the end): no destination
-        if (slot[u] >= p.num_slots) {
-          if (p.err && j0 == 0) atomicOr(p.err, kErrSlot);
-          continue;
-        }
-        const int64_t blk = slot[u] / kBlock, off = slot[u] % kBlock;
-        char *kd = static_cast<char *>(p.k_cache) + (blk * p.kc_s0 + hcur * p.kc_s1 + off * p.kc_s2 + e) * CB;
-        char *vd = static_cast<char *>(p.v_cache) + (blk * p.vc_s0 + hcur * p.vc_s1 + off * p.vc_s2 + e) * CB;
-        if constexpr (!FP8) {
-          *reinterpret_cast<uint4 *>(kd) = kv[u];
-          *reinterpret_cast<uint4 *>(vd) = vv[u];
-        } else {
-          store_fp8<DT>(kd, kv[u], kdiv);
-          store_fp8<DT>(vd, vv[u], vdiv);
-        }
+      char *kd, *vd;
+      if constexpr (I32) {
+        const int blk = static_cast<int>(slot >> 4), off = static_cast<int>(slot & 15);
+        kd = static_cast<char *>(p.k_cache) + static_cast<int64_t>(blk) * static_cast<int>(p.kc_s0 * CB) +
+             (static_cast<int>(kin) + off * static_cast<int>(p.kc_s2 * CB));
+        vd = static_cast<char *>(p.v_cache) + static_cast<int64_t>(blk) * static_cast<int>(p.vc_s0 * CB) +
+             (static_cast<int>(vin) + off * static_cast<int>(p.vc_s2 * CB));
+      } else {
+        const int64_t blk = slot / kBlock, off = slot % kBlock;
+        kd = static_cast<char *>(p.k_cache) + (blk * p.kc_s0 + off * p.kc_s2) * CB + kin;
+        vd = static_cast<char *>(p.v_cache) + (blk * p.vc_s0 + off * p.vc_s2) * CB + vin;
       }
+      if constexpr (!FP8) {
+        *reinterpret_cast<uint4 *>(kd) = kv;
+        *reinterpret_cast<uint4 *>(vd) = vv;
+      } else {
+        store_fp8<DT>(kd, kv, kdiv);
+        store_fp8<DT>(vd, vv, vdiv);
+      }
+    };
+    auto src = [&](const char *base, int64_t tt, int64_t ts) {
+      if constexpr (I32) return base + static_cast<int>(tt) * static_cast<int>(ts * IB);
+      else return base + tt * ts * IB;
+    };
+    int64_t t = static_cast<int64_t>(blockIdx.x) * rows + tl;
+    int64_t slot = -1;
+    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+    if (t < p.T) {
+      slot = __ldg(p.slot_mapping + t);
+      kv = ld_once(src(ks, t, p.key_ts));
+      vv = ld_once(src(vs, t, p.val_ts));
+    }
+    while (t < p.T) {
+      const int64_t tn = t + stride;
+      int64_t slot_n = -1;
+      uint4 kvn = kv, vvn = vv;
+      if (tn < p.T) {
+        slot_n = __ldg(p.slot_mapping + tn);
+        kvn = ld_once(src(ks, tn, p.key_ts));
+        vvn = ld_once(src(vs, tn, p.val_ts));
+      }
+      process(slot, kv, vv);
+      t = tn;
+      slot = slot_n;
+      kv = kvn;
+      vv = vvn;
     }
     return;
   }
@@ -252,15 +315,16 @@ cudaError_t launch_one(const WriteParams &p, int sm_count, cudaStream_t st) {
   const int per_tok = p.Hkv * (p.D / EPP);
   const int rows = 256 / (per_tok < 256 ? per_tok : 256);
   int64_t blocks = (p.T + rows - 1) / rows;
-  const int64_t cap = static_cast<int64_t>(sm_count) * 8;  // 8 x 256 threads per SM, grid-stride
+  const int64_t cap = static_cast<int64_t>(sm_count) * kWriteCtasPerSm;  // one resident wave, grid-stride
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   // the write uses no shared memory and reads around L1; keep the SM's shared/L1 split the
   // decode kernels ask for, so the usual write -> decode sequence does not reconfigure it
-  cudaError_t e = cudaFuncSetAttribute(write_kernel<DT, FP8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  auto kern = p.i32 ? write_kernel<DT, FP8, true> : write_kernel<DT, FP8, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  write_kernel<DT, FP8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  kern<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

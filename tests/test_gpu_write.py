@@ -179,3 +179,58 @@ def test_empty_write_is_a_no_op():
     pa.pa_reshape_and_cache(e, e, kc, kc.clone(), torch.empty(0, dtype=torch.int64, device="cuda"))
     torch.cuda.synchronize()
     assert not kc.view(torch.int16).any()
+
+
+@pytest.mark.parametrize("scales", ["tensor", "heads", "odd"])
+@pytest.mark.parametrize("in_dt", ["bf16", "f16"])
+@pytest.mark.parametrize("H,D", [(8, 128), (2, 64), (24, 256)], ids=["8x128", "2x64", "24x256"])
+def test_fp8_write_all_16bit_patterns(H, D, in_dt, scales):
+    """Every bf16 / f16 bit pattern (zeros, subnormals, infinities, NaN, magnitudes beyond
+    2^80 and below 2^-80 among them) through the E4M3 write, bit for bit against the oracle:
+    token shapes that fit one block of threads and wider ones, one scale per tensor, one per
+    KV head, or unusual ones (a negative scale; a scale below 2^-40, which takes the IEEE
+    division), padding rows skipped."""
+    per_head = scales == "heads"
+    rng = np.random.default_rng(H * 1000 + D)
+    n = H * D
+    T = (65536 + n - 1) // n + 3
+    pats = np.zeros(T * n, dtype=np.uint16)
+    pats[:65536] = rng.permutation(65536).astype(np.uint16)
+    kbits = pats.reshape(T, H, D)
+    vbits = rng.permutation(pats).reshape(T, H, D)
+    tdt = torch.bfloat16 if in_dt == "bf16" else torch.float16
+    key = torch.from_numpy(kbits.view(np.int16).copy()).view(tdt)
+    val = torch.from_numpy(vbits.view(np.int16).copy()).view(tdt)
+    NB = (T + 15) // 16 + 2
+    slots = rng.permutation(NB * B)[:T].astype(np.int64)
+    pad = rng.choice(T, size=2, replace=False)
+    slots[pad] = -1
+    if scales == "heads":
+        ks = (0.05 * (1 + np.arange(H) / 8)).astype(np.float32)
+        vs = (0.9 / (1 + np.arange(H))).astype(np.float32)
+    elif scales == "odd":
+        ks, vs = np.float32(-0.05), np.float32(2.0 ** -45)
+    else:
+        ks, vs = np.float32(0.05), np.float32(3.0)
+    dev = "cuda"
+    kc = torch.full((NB, H, B, D), 0xFF, dtype=torch.uint8, device=dev)
+    vc = torch.full((NB, H, B, D), 0xFF, dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pa.pa_reshape_and_cache_opt(key.to(dev), val.to(dev), kc, vc, torch.from_numpy(slots).to(dev),
+                                pa.PA_KV_FP8_E4M3, torch.tensor(np.atleast_1d(ks), device=dev),
+                                torch.tensor(np.atleast_1d(vs), device=dev), 1 if per_head else 0, err)
+    rc, bits = pa.pa_check_device_error(err)
+    assert rc == 0, bits
+    for cache, src, sc in ((kc, kbits, ks), (vc, vbits, vs)):
+        ref = oracle_write(src, in_dt, slots, NB, np.uint8, "e4m3", sc)
+        got = flat_view(cache)
+        x = (src.astype(np.uint32) << 16).view(np.float32) if in_dt == "bf16" else src.view(np.float16)
+        nan_rows = np.isnan(x)
+        written = slots[slots >= 0]
+        rows = np.nonzero(slots >= 0)[0]
+        g, r = got[written], ref[written]
+        nan_in = nan_rows[rows]
+        assert np.all((g[nan_in] & 0x7F) == 0x7F) and np.all((r[nan_in] & 0x7F) == 0x7F)
+        assert np.array_equal(g[~nan_in], r[~nan_in])
+        untouched = np.setdiff1d(np.arange(NB * B), written)
+        assert np.all(got[untouched] == 0xFF)
