@@ -157,6 +157,34 @@ __host__ __device__ constexpr uint32_t idesc(bool bf, bool b_mn_major, int M, in
 
 }  // namespace umma
 
+// Packed fp32 pairs (one 64-bit register pair, low half first) and the two-lane
+// round-to-nearest arithmetic on them; a three-input max.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 constexpr uint32_t kUmmaWaitLimit = 1u << 20;  // mbarrier polls before a wait gives up
 constexpr float kUmmaSlack = 8.f;              // lazy running max, log2 units (p <= 256)
 constexpr float kUmmaEmpty = -1e30f;           // running max of a row with no visible token yet
@@ -430,13 +458,18 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
         for (int i = 0; i < 64; ++i)
           x[i] = i <= lim ? fmaf(x[i], p.scale_log2, fmaf(ab, static_cast<float>(i), base)) : -INFINITY;
       }
-      float mx[8];
+      // row max of the group: a tree of three-input max instructions
+      float lm;
+      {
+        float a[22], b[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(x[j], x[j + 8]), fmaxf(x[j + 16], x[j + 24]));
+        for (int i = 0; i < 21; ++i) a[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+        a[21] = x[63];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], fmaxf(fmaxf(x[j + 32], x[j + 40]), fmaxf(x[j + 48], x[j + 56])));
-      const float lm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-                       (raw ? p.scale_log2 : 1.f);
+        for (int i = 0; i < 7; ++i) b[i] = fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+        b[7] = a[21];
+        lm = fmax3(fmax3(b[0], b[1], b[2]), fmax3(b[3], b[4], b[5]), fmaxf(b[6], b[7])) * (raw ? p.scale_log2 : 1.f);
+      }
       const float sc = raw ? p.scale_log2 : 1.f;  // p = exp2(x sc - m)
       const bool need = lm > m + kUmmaSlack;
       const float mn = need ? lm : m;
@@ -463,27 +496,36 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
         umma::wait_st();
       }
       m = mn;
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // probabilities two at a time: exponent arguments and the row sum as packed fp32 pairs,
+      // each P pair split into its 16-bit hi half and the rounded remainder (lo)
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+      const uint64_t sc2 = f2pack(sc, sc), nm2 = f2pack(-m, -m), neg1 = f2pack(-1.f, -1.f);
 #pragma unroll
       for (int pg = 0; pg < C::GP; ++pg) {
         uint32_t w[16];  // 8 hi words, then 8 lo words, of the page's 16 tokens
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float u = ex2(fmaf(x[16 * pg + 2 * i], sc, -m)), v = ex2(fmaf(x[16 * pg + 2 * i + 1], sc, -m));
-          ls[i] += u + v;
+          const float2 e = f2unpack(f2fma(f2pack(x[16 * pg + 2 * i], x[16 * pg + 2 * i + 1]), sc2, nm2));
+          const float u = ex2(e.x), v = ex2(e.y);
+          const uint64_t uv = f2pack(u, v);
+          ls2[i & 3] = f2add(ls2[i & 3], uv);
+          float2 f;
           if constexpr (C::BF) {
             w[i] = pack_bf16(u, v);
-            const float2 f = unpack_bf16(w[i]);
-            w[8 + i] = pack_bf16(u - f.x, v - f.y);
+            f = unpack_bf16(w[i]);
           } else {
             w[i] = pack_f16(u, v);
-            const float2 f = unpack_f16(w[i]);
-            w[8 + i] = pack_f16(u - f.x, v - f.y);
+            f = unpack_f16(w[i]);
           }
+          const float2 r = f2unpack(f2fma(f2pack(f.x, f.y), neg1, uv));  // (u, v) - hi, exact
+          w[8 + i] = C::BF ? pack_bf16(r.x, r.y) : pack_f16(r.x, r.y);
         }
         umma::st16(tl + 64u * b + 16u * pg, w);
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      {
+        const float2 a = f2unpack(f2add(ls2[0], ls2[1])), c = f2unpack(f2add(ls2[2], ls2[3]));
+        l += (a.x + a.y) + (c.x + c.y);
+      }
       umma::wait_st();
       if (!waited && !__all_sync(0xffffffffu, umma_wait(odone(tile), (k - 1) & 1, abort))) {
         ok = false;
