@@ -11,8 +11,9 @@
 // token and pack indices are fixed and the loop is a stride over tokens; each
 // destination (block, head, offset) row is a contiguous run of D * elem bytes in
 // the HND cache, so a warp's stores cover whole 32-byte sectors.  Sources are read
-// once with no L1 allocation.  The grid is at most 8 CTAs per SM, grid-striding
-// over tokens.  The E4M3 path divides by the tensor's scale, or its KV head's
+// once with no L1 allocation.  The grid is one resident wave (4 CTAs per SM) striding
+// over tokens, each thread streaming its tokens through a two-deep software pipeline.
+// The E4M3 path divides by the tensor's scale, or its KV head's
 // (Part 2: kv_scale_stride == 0 shares one scale, otherwise head h uses
 // scale[h * kv_scale_stride]), with a reciprocal-based, correctly rounded quotient
 // (Divisor below), the same value as an IEEE division.
@@ -173,13 +174,11 @@ __device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, const Divis
   }
 }
 
-// Token turns per thread whose loads are issued together.  Measured on GB300 against one
-// turn at a time: 2 turns cut a 1024-row write from 7.6-8.1 to 6.3 us and leave the
-// 8192-row E4M3 chunk (ALU-bound) at 18.4 us; 4 turns needed 80 registers (3 CTAs per SM)
-// and slowed the chunk to 20.5 us.
-constexpr int kBatch = 2;
 // CTAs per SM of the grid: the resident ones (the launch bound), so that every CTA is in
-// flight from the start and streams its tokens through the software pipeline.
+// flight from the start and streams its tokens through the software pipeline.  Measured on
+// GB300 against the 8192-row E4M3 chunk: this one wave with a two-deep pipeline 14.7 us;
+// two batched turns per thread over two waves 18.5 us; a three-deep pipeline (3 CTAs per SM)
+// no faster; 5 or 6 CTAs per SM (registers spill) 16.5 / 18.4 us.
 constexpr int kWriteCtasPerSm = 4;
 
 template <int DT, bool FP8, bool I32>
@@ -209,10 +208,7 @@ __global__ void __launch_bounds__(256, 4) write_kernel(const WriteParams p) {
   }
   const int64_t stride = static_cast<int64_t>(gridDim.x) * rows;  // tokens between a thread's turns
   if (per_tok <= 256) {
-    // The thread's pack is fixed (head hcur, element e).  Tokens go in batches of kBatch
-    // turns: the slot and both source packs of every turn are loaded before any conversion
-    // or store, so one memory round trip covers the batch.  (Padding rows are loaded too;
-    // their sources are in bounds and nothing is written for them.)
+    // The thread's pack is fixed (head hcur, element e).
     const int64_t e = static_cast<int64_t>(j0 - hcur * ppr) * EPP;
     const char *ks = static_cast<const char *>(p.key) + (hcur * p.key_hs + e) * IB;
     const char *vs = static_cast<const char *>(p.value) + (hcur * p.val_hs + e) * IB;
