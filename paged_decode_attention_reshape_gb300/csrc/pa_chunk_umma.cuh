@@ -31,8 +31,9 @@
 // Synchronisation (mbarriers, every wait bounded and abandoned when another role gave
 // up): full[slot] (TMA bytes) -> the issuers; per tile s_full[b] (commit) -> softmax,
 // p_full[b] (128 arrivals) -> its issuer, o_done (commit after each group's P.V) ->
-// softmax, which waits for every group in turn (an O rescale needs it, and the parity
-// waits stay one phase apart); empty[slot] (one commit per active tile) -> TMA.  The MMAs
+// softmax, only before an O rescale and the epilogue (S of group k is issued after P.V of
+// group k - 2, so its completion bounds o_done's phase from below and a parity wait cannot
+// be a phase off); empty[slot] (one commit per active tile) -> TMA.  The MMAs
 // of one issuer run in order, so S of group k + 2 may overwrite the P that P.V of group k
 // reads.  Tile 0 zeroes the V rows past the sequence in the last page before it hands over
 // its P; the other tiles' last P.V also waits for that hand-over.
@@ -332,18 +333,18 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
     const int32_t *bt = p.block_table + static_cast<int64_t>(s) * p.bt_ss;
     const uint64_t pol = policy_evict_normal();  // the other row tiles of (s, g) read the same pages
     const int c1 = p.nhd ? g : 0, c2 = p.nhd ? 0 : g;
+    // block-table entries are read one group ahead, off the path from a free slot to its copies
+    int pid_next = lane < min(C::GP, npages) ? __ldg(bt + lane) : 0;
     for (int k = 0; k < ngr; ++k) {
       const int gs = k % C::NS;
       if (k >= C::NS && !__all_sync(0xffffffffu, umma_wait(empty0 + 8 * gs, ((k / C::NS) - 1) & 1, abort))) break;
       const int npg = min(C::GP, npages - k * C::GP);
-      int pid = 0;
-      if (lane < npg) {
-        pid = __ldg(bt + k * C::GP + lane);
-        if (pid < 0 || pid >= p.num_blocks) {
-          *bad_block = 1;
-          if (p.err) atomicOr(p.err, kErrBlock);
-          pid = 0;  // load a valid block; the CTA writes nothing
-        }
+      int pid = pid_next;
+      if (k + 1 < ngr) pid_next = lane < min(C::GP, npages - (k + 1) * C::GP) ? __ldg(bt + (k + 1) * C::GP + lane) : 0;
+      if (lane < npg && (pid < 0 || pid >= p.num_blocks)) {
+        *bad_block = 1;
+        if (p.err) atomicOr(p.err, kErrBlock);
+        pid = 0;  // load a valid block; the CTA writes nothing
       }
       if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * gs, npg * 2 * C::NBOX * C::BOXB);
       __syncwarp();
@@ -473,15 +474,14 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       const float sc = raw ? p.scale_log2 : 1.f;  // p = exp2(x sc - m)
       const bool need = lm > m + kUmmaSlack;
       const float mn = need ? lm : m;
-      // P.V of the previous group must have completed before O is rescaled; every group
-      // waits for it once (below at the latest) so that the parity waits stay in step
-      bool waited = k == 0;
+      // P.V of the previous group must have completed before O is rescaled.  The wait is
+      // unambiguous without one in every group: S(k) was issued after P.V(k - 2), so its
+      // completion means at least k - 1 phases of o_done, and P.V(k) needs this group's P
       if (k >= 1 && __any_sync(0xffffffffu, need)) {
         if (!__all_sync(0xffffffffu, umma_wait(odone(tile), (k - 1) & 1, abort))) {
           ok = false;
           break;
         }
-        waited = true;
         umma::fence_after();
         const float al = ex2(m - mn);
         l *= al;
@@ -527,10 +527,6 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
         l += (a.x + a.y) + (c.x + c.y);
       }
       umma::wait_st();
-      if (!waited && !__all_sync(0xffffffffu, umma_wait(odone(tile), (k - 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
       if (k == ngr - 1 && tile == 0) {
         // V rows of tokens >= len in the last page may hold anything (NaN included) and
         // P . V would carry it into O even with P = 0 there: tile 0 zeroes them before it
