@@ -115,8 +115,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 4-D map over a [NB, Hkv, 16, D] cache: dims (D, 16, Hkv, NB), box (128 bytes, 16, 1, 1),
-// 128-byte swizzle.  One box = 16 token rows x 128 bytes = 2 KiB of one page.
 // 4-D TMA map of one cache, boxes of one (block, kv head) page: 16 token rows of one
 // 128-byte swizzle span.  HND caches (token stride <= head stride) are described as
 // (D, 16, Hkv, NB), box (span, 16, 1, 1); NHD caches (token-major within a block,
@@ -139,6 +137,28 @@ int make_cache_map(const pa_tensor *c, CUtensorMap *map, int *nhd) {
   const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   CUresult r = enc(map, dt, 4, c->data, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// 3-D TMA map of varlen queries [Tq, Hq, D] for the query-tile kernel: dims (D, Hq, Tq),
+// box (64 elements, G heads, 128 / G tokens), 128-byte swizzle.  One box is 128 rows (query
+// token-major, head-minor: the kernel's row order) of one 128-byte column span, the layout
+// in which the kernel's MMAs read Q.  Needs G to divide 128; PA_ERR_INVALID_ARG otherwise
+// (the kernel then loads Q itself).  The strides were checked 16-byte aligned by the caller.
+int make_q_map(const pa_tensor *q, int G, CUtensorMap *map) {
+  if (G <= 0 || 128 % G != 0) return PA_ERR_INVALID_ARG;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PA_ERR_CUDA;
+  const int eb = elem_bytes(q->dtype);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(q->shape[2]), static_cast<cuuint64_t>(q->shape[1]),
+                              static_cast<cuuint64_t>(q->shape[0])};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(q->stride[1] * eb), static_cast<cuuint64_t>(q->stride[0] * eb)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(G),
+                             static_cast<cuuint32_t>(128 / G)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, q->data, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -647,9 +667,15 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
     if (nhd_k != nhd_v) return PA_ERR_INVALID_ARG;  // K and V in different layouts
     p.nhd = nhd_k;
     ProfScope ps(PA_KERNEL_DECODE, st);
-    if (chunk) e = launch_chunk_umma(p, kind, tmK, tmV, st);
-    else if (kind == KIND_BF16 || kind == KIND_F16) e = launch_decode_mma_16(p, kind, tmK, tmV, st);
-    else e = launch_decode_mma_fp8(p, kind, tmK, tmV, st);
+    if (chunk) {
+      CUtensorMap tmQ{};
+      p.q_tma = make_q_map(q, p.G, &tmQ) == PA_OK ? 1 : 0;
+      e = launch_chunk_umma(p, kind, tmK, tmV, tmQ, st);
+    } else if (kind == KIND_BF16 || kind == KIND_F16) {
+      e = launch_decode_mma_16(p, kind, tmK, tmV, st);
+    } else {
+      e = launch_decode_mma_fp8(p, kind, tmK, tmV, st);
+    }
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -209,8 +209,9 @@ struct UmmaCfg {
   static constexpr int QTILE = NBOX * QBOX;           // one Q tile
   static constexpr int RING = R * BOXB;               // one box region of a ring
   static constexpr int QOFF = 0, KOFF = T * QTILE, VOFF = KOFF + NBOX * RING, BAR_OFF = VOFF + NBOX * RING;
-  // barriers: full[NS], empty[NS]; per tile s_full x2, p_full x2, o_done, drain (48 bytes)
-  static constexpr int TBAR = 2 * NS * 8, NBARS = 2 * NS + 6 * T;
+  // barriers: full[NS], empty[NS]; per tile s_full x2, p_full x2, o_done, drain (48 bytes);
+  // q_full
+  static constexpr int TBAR = 2 * NS * 8, NBARS = 2 * NS + 6 * T + 1;
   static constexpr size_t SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 256 * T;      // tile t: S/P buffers at 256 t + 0 / 64, O at 256 t + 128
   static constexpr uint32_t OCOL = 128;
@@ -232,7 +233,7 @@ __device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, volatil
 template <int KIND, int D, int T>
 __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D, T>::MIN_CTAS)
     chunk_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmQ) {
   using C = UmmaCfg<KIND, D, T>;
   using OutT = typename std::conditional<C::BF, __nv_bfloat16, __half>::type;
   extern __shared__ uint8_t smem_raw[];
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   auto pfull = [&](int t, int b) { return tbar0 + 48u * t + 16u + 8u * b; };
   auto odone = [&](int t) { return tbar0 + 48u * t + 32u; };
   auto drain = [&](int t) { return tbar0 + 48u * t + 40u; };
+  const uint32_t qfull = tbar0 + 48u * T;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + C::BAR_OFF + C::NBARS * 8);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *bad_block = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   if (tid == 0) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
+    if (p.q_tma) prefetch_tensormap(&tmQ);
   }
   grid_dependency_wait();
 
@@ -288,13 +291,18 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       mbar_init(odone(t), 1);
       mbar_init(drain(t), 1);
     }
+    mbar_init(qfull, 1);
     *abort = 0;
     *bad_block = 0;
     fence_barrier_init();
   }
+  // The barriers are initialised: the TMA producer starts on Q and the first K/V pages now,
+  // the other roles meet again below once TMEM is allocated (and Q is stored, without TMA).
+  __syncthreads();
 
-  // ---- Q tiles -> shared memory (128-byte swizzle, the layout TMA would give), zero rows past nrows
-  if (tid < C::ROWS) {
+  // ---- Q tiles -> shared memory by the softmax threads when there is no Q tensor map:
+  // the 128-byte swizzle TMA gives, zero rows past nrows
+  if (!p.q_tma && tid < C::ROWS) {
     const int r = r0 + tid, tr = tid & 127;
     const bool valid = tid < nrows;
     const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -313,10 +321,13 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
     umma::tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     umma::tmem_relinquish();
   }
-  umma::fence_before();
-  __syncthreads();
-  umma::fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  if (warp != C::TMA_WARP) {
+    // every role but the producer: the TMEM address and a Q the threads stored (named barrier 1)
+    umma::fence_before();
+    asm volatile("bar.sync 1, %0;" ::"r"(C::THREADS - 32) : "memory");
+    umma::fence_after();
+  }
+  const uint32_t tmem = warp == C::TMA_WARP ? 0u : *reinterpret_cast<volatile uint32_t *>(tmem_slot);
 
   // softmax state of row r0 + tid (threads below ROWS: tile tid / 128), kept for the epilogue
   const int row = r0 + tid;
@@ -335,6 +346,16 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
     const int c1 = p.nhd ? g : 0, c2 = p.nhd ? 0 : g;
     // block-table entries are read one group ahead, off the path from a free slot to its copies
     int pid_next = lane < min(C::GP, npages) ? __ldg(bt + lane) : 0;
+    if (p.q_tma && lane == 0) {
+      // Q first: the row tiles' boxes (query tokens x G heads x 64 dims each); rows past nrows
+      // hold other tokens or zeros, and only feed rows that are never stored
+      mbar_arrive_expect_tx(qfull, ntiles * C::NBOX * C::QBOX);
+      const uint64_t qpol = policy_evict_first();
+      for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+        for (int bx = 0; bx < C::NBOX; ++bx)
+          tma_load_3d(qs + t * C::QTILE + bx * C::QBOX, &tmQ, qfull, bx * 64, g * G, a + (r0 + 128 * t) / G, qpol);
+    }
     for (int k = 0; k < ngr; ++k) {
       const int gs = k % C::NS;
       if (k >= C::NS && !__all_sync(0xffffffffu, umma_wait(empty0 + 8 * gs, ((k / C::NS) - 1) & 1, abort))) break;
@@ -381,6 +402,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
                                    ? (p.first_wait_limit < 0 ? 0u : static_cast<uint32_t>(p.first_wait_limit))
                                    : kUmmaWaitLimit;
           if (!__all_sync(0xffffffffu, umma_wait(full0 + 8 * gs, (k / C::NS) & 1, abort, lim))) break;
+          if (k == 0 && p.q_tma && !__all_sync(0xffffffffu, umma_wait(qfull, 0, abort))) break;
           umma::fence_after();
           const uint64_t kd = kd0 + ((gs * C::GP * C::BOXB) >> 4);
           if (elect_one()) {
@@ -556,9 +578,11 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
     // each MMA issuer for the completion of every MMA it issued, before the shared memory and
     // the tensor memory are released.
     if (warp == C::TMA_WARP) {
-      if (lane == 0)
+      if (lane == 0) {
         for (int k2 = max(0, issued - C::NS); k2 < issued; ++k2)
           mbar_wait_bounded(full0 + 8 * (k2 % C::NS), (k2 / C::NS) & 1, kUmmaWaitLimit);
+        if (p.q_tma) mbar_wait_bounded(qfull, 0, kUmmaWaitLimit);
+      }
     } else if (warp >= C::MMA_WARP && warp - C::MMA_WARP < ntiles) {
       const int t = warp - C::MMA_WARP;
       if (elect_one()) umma::commit(drain(t));  // arrives once every MMA of this issuer has completed
@@ -602,7 +626,8 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
 template <int KIND, int D, int T>
 struct UmmaLaunch {
   using C = UmmaCfg<KIND, D, T>;
-  static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV, cudaStream_t st) {
+  static cudaError_t launch(const DecodeParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                            const CUtensorMap &tmQ, cudaStream_t st) {
     auto kern = chunk_umma_kernel<KIND, D, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
@@ -610,7 +635,7 @@ struct UmmaLaunch {
     if (e != cudaSuccess) return e;
     const int rows = p.nq_max * p.G;
     const dim3 grid((rows + C::ROWS - 1) / C::ROWS, p.Hkv, p.S);
-    e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, 1, p, tmK, tmV);
+    e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, st, 1, p, tmK, tmV, tmQ);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
 };

@@ -68,6 +68,7 @@ struct DecodeParams {
   int64_t Tq;                          // rows of q / out
   int VH;                              // virtual heads per KV head; HG = ceil(VH / 8)
   int nhd;                             // caches token-major within a block (TMA coordinates (d, g, 0, blk))
+  int q_tma;                           // query-tile kernel: Q tiles come by TMA (tmQ), else by loads
   // Early reads (pa_decode_step): the grid launched just before this one writes only the
   // newest n_s positions of each sequence s (n_s = new_start[s+1] - new_start[s], or 1 when
   // new_start is null).  The kernel then reads q, the tables and every other page before that
@@ -151,8 +152,9 @@ cudaError_t launch_decode_mma_fp8(const DecodeParams &p, int kind, const CUtenso
 cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st);
 // Query-tile kernel for chunks of query tokens (pa_attention_varlen) on tcgen05 tensor
 // cores: bf16 / f16 caches, head sizes 64 and 128; never splits the page range.
+// tmQ is read when p.q_tma is set (make_q_map).
 cudaError_t launch_chunk_umma(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                              cudaStream_t st);
+                              const CUtensorMap &tmQ, cudaStream_t st);
 // Query columns per KV head (max_query_len x G) from which varlen attention uses it: below
 // 64 columns the column-group kernels are as fast or faster.
 constexpr int kChunkMinColumns = 64;
