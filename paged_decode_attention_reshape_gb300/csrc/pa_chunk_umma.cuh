@@ -591,25 +591,49 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
     }
   }
   if (warp < 4 * T && tile < ntiles) {
-    // ---- epilogue: O / l -> out
+    // ---- epilogue: O / l -> out, staged in the tile's Q tile (free once the tile's last MMA
+    // has completed) so that the copy to out writes whole rows with consecutive lanes
+    uint8_t *stage = sgen + C::QOFF + tile * C::QTILE;
     if (ok && __all_sync(0xffffffffu, umma_wait(odone(tile), (ngr - 1) & 1, abort))) {
       umma::fence_after();
-      const bool store = valid && !*bad_block;
+      const int rr = tid & 127;  // this thread's row within the tile
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      OutT *dst = static_cast<OutT *>(p.out) +
-                  (static_cast<int64_t>(a) + row / G) * p.out_ss + static_cast<int64_t>(g * G + row % G) * p.out_hs;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         umma::ld32(tl + C::OCOL + 32u * c, o);
-        if (store) {
-          uint32_t w[16];
+        uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = C::BF ? pack_bf16(o[2 * i] * inv, o[2 * i + 1] * inv) : pack_f16(o[2 * i] * inv, o[2 * i + 1] * inv);
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+        for (int i = 0; i < 16; ++i)
+          w[i] = C::BF ? pack_bf16(o[2 * i] * inv, o[2 * i + 1] * inv) : pack_f16(o[2 * i] * inv, o[2 * i + 1] * inv);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) {
+          const int ch = 4 * c + i;  // 16-byte chunk of the row, 128-byte swizzle as for Q
+          *reinterpret_cast<uint4 *>(stage + (ch >> 3) * C::QBOX + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                                     (((ch & 7) ^ (rr & 7)) << 4)) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+    }
+    // all four warps of the tile arrive here (named barrier 2 + tile); without an abort every
+    // one of them staged its rows
+    if (tile == 0)
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+    else
+      asm volatile("bar.sync 3, 128;" ::: "memory");
+    if (!*abort && !*bad_block) {
+      constexpr int CPR = D / 8;  // 16-byte chunks per row: a warp writes 512 contiguous bytes per step
+      const int wl = tid & 127;
+#pragma unroll 4
+      for (int it = 0; it < CPR; ++it) {
+        const int idx = it * 128 + wl, rr = idx / CPR, ch = idx % CPR;
+        const int r = r0 + tile * 128 + rr;  // row of the KV head
+        if (r - r0 < nrows) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(stage + (ch >> 3) * C::QBOX + (rr >> 3) * 1024 +
+                                                           (rr & 7) * 128 + (((ch & 7) ^ (rr & 7)) << 4));
+          OutT *dst = static_cast<OutT *>(p.out) +
+                      (static_cast<int64_t>(a) + r / G) * p.out_ss + static_cast<int64_t>(g * G + r % G) * p.out_hs;
+          reinterpret_cast<uint4 *>(dst)[ch] = v;
         }
       }
     }
