@@ -348,9 +348,11 @@ PA_API const char *pa_status_string(int status) {
   }
 }
 
-PA_API int pa_reshape_and_cache_opt(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache,
-                                    pa_tensor *v_cache, const pa_tensor *slot_mapping, int kv_dtype,
-                                    const pa_write_options *opt, pa_stream_t stream) {
+// The write with its grid's CTAs per SM (0: the standalone choice; pa_decode_step asks for
+// fewer when the decode's early reads overlap it).
+static int write_impl(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache, pa_tensor *v_cache,
+                      const pa_tensor *slot_mapping, int kv_dtype, const pa_write_options *opt, pa_stream_t stream,
+                      int ctas_per_sm) {
   const pa_write_options o = opt ? *opt : pa_write_options{};
   if (o.scale_stride < 0) return PA_ERR_INVALID_ARG;
   int r;
@@ -422,9 +424,15 @@ PA_API int pa_reshape_and_cache_opt(const pa_tensor *key, const pa_tensor *value
   cudaError_t e;
   {
     ProfScope ps(PA_KERNEL_WRITE, st);
-    e = launch_write(p, in_dt, k_cache->dtype, sm, st);
+    e = launch_write(p, in_dt, k_cache->dtype, sm, ctas_per_sm, st);
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API int pa_reshape_and_cache_opt(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache,
+                                    pa_tensor *v_cache, const pa_tensor *slot_mapping, int kv_dtype,
+                                    const pa_write_options *opt, pa_stream_t stream) {
+  return write_impl(key, value, k_cache, v_cache, slot_mapping, kv_dtype, opt, stream, 0);
 }
 
 PA_API int pa_reshape_and_cache(const pa_tensor *key, const pa_tensor *value, pa_tensor *k_cache, pa_tensor *v_cache,
@@ -755,10 +763,13 @@ PA_API int pa_decode_step(pa_tensor *out, const pa_tensor *q, const pa_tensor *k
     return r;
   const pa_write_options wo{o.k_scale, o.v_scale, o.scale_stride, o.device_error};
   const int kv = k_cache->dtype == PA_FP8_E4M3 ? PA_KV_FP8_E4M3 : PA_KV_AUTO;
-  if ((r = pa_reshape_and_cache_opt(key, value, k_cache, v_cache, slot_mapping, kv, &wo, stream))) return r;
   // Early reads pay when the write is long (several new rows per sequence: measured 202.8 ->
   // 198.7 us on 128 sequences x 64 rows into an E4M3 cache); a one-row write is over before
-  // they help, and the early variant's in-loop wait costs more (c2: 33.3 vs 33.5 us).
+  // they help, and the early variant's in-loop wait costs more (c2: 33.3 vs 33.5 us).  With
+  // early reads the write takes two CTAs per SM, leaving the decode's CTAs room beside it
+  // (same step, graph replay: 4 / 3 / 2 / 1 write CTAs per SM 195.5 / 192.7 / 191.0 / 194.9 us).
+  const int write_ctas = new_rows_start ? 2 : 0;
+  if ((r = write_impl(key, value, k_cache, v_cache, slot_mapping, kv, &wo, stream, write_ctas))) return r;
   return decode_impl(out, q, k_cache, v_cache, block_table, seq_lens, scale, num_kv_heads, o, internal, stream,
                      nullptr, 1, new_rows_start, new_rows_start != nullptr);
 }

@@ -118,7 +118,9 @@ int decode_ex_requirements(pa_tensor *out, const pa_tensor *q, const pa_tensor *
                            size_t *ws_bytes, size_t *counter_bytes);
 
 // Launchers (defined next to their kernels).  Return a cudaError_t.
-cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, int sm_count, cudaStream_t st);
+// ctas_per_sm: the grid's CTAs per SM (1 .. 4; 0 = the standalone write's choice).
+cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, int sm_count, int ctas_per_sm,
+                         cudaStream_t st);
 
 // Tensor-core kernel shape per (kind, head size): warps per CTA and pipeline
 // stages per warp.  Shared memory = W * STAGES * 2 pages (+ alignment, barriers).

@@ -174,12 +174,14 @@ __device__ __forceinline__ void store_fp8(char *dst, const uint4 &v, const Divis
   }
 }
 
-// CTAs per SM of the grid: the resident ones (the launch bound), so that every CTA is in
-// flight from the start and streams its tokens through the software pipeline.  Measured on
-// GB300 against the 8192-row E4M3 chunk: this one wave with a two-deep pipeline 14.7 us;
-// two batched turns per thread over two waves 18.5 us; a three-deep pipeline (3 CTAs per SM)
-// no faster; 5 or 6 CTAs per SM (registers spill) 16.5 / 18.4 us.
-constexpr int kWriteCtasPerSm = 4;
+// CTAs per SM of the grid (at most the resident ones, the launch bound), so that every CTA
+// is in flight from the start and streams its tokens through the software pipeline.
+// Measured on GB300, two-deep pipeline: the 8192-row E4M3 chunk with 1, 2, 3, 4 CTAs per SM
+// 23.9, 16.5, 14.8, 15.4 us, the 32768-row bf16 copy with 3 or 4 45.5 / 43.9 us; two batched
+// turns per thread over two waves 18.5 us; a three-deep pipeline no faster; 5 or 6 CTAs per SM
+// (registers spill) 16.5 / 18.4 us.  (pa_decode_step asks for fewer when the decode overlaps
+// the write.)
+constexpr int kWriteCtasPerSmFp8 = 3, kWriteCtasPerSmCopy = 4;
 
 template <int DT, bool FP8, bool I32>
 __global__ void __launch_bounds__(256, 4) write_kernel(const WriteParams p) {
@@ -306,12 +308,13 @@ __global__ void __launch_bounds__(256, 4) write_kernel(const WriteParams p) {
 }
 
 template <int DT, bool FP8>
-cudaError_t launch_one(const WriteParams &p, int sm_count, cudaStream_t st) {
+cudaError_t launch_one(const WriteParams &p, int sm_count, int ctas_per_sm, cudaStream_t st) {
   constexpr int EPP = 16 / In<DT>::bytes;
   const int per_tok = p.Hkv * (p.D / EPP);
   const int rows = 256 / (per_tok < 256 ? per_tok : 256);
   int64_t blocks = (p.T + rows - 1) / rows;
-  const int64_t cap = static_cast<int64_t>(sm_count) * kWriteCtasPerSm;  // one resident wave, grid-stride
+  const int per_sm = ctas_per_sm > 0 && ctas_per_sm <= 4 ? ctas_per_sm : FP8 ? kWriteCtasPerSmFp8 : kWriteCtasPerSmCopy;
+  const int64_t cap = static_cast<int64_t>(sm_count) * per_sm;  // one resident wave, grid-stride
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   // the write uses no shared memory and reads around L1; keep the SM's shared/L1 split the
@@ -326,12 +329,14 @@ cudaError_t launch_one(const WriteParams &p, int sm_count, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, int sm_count, cudaStream_t st) {
+cudaError_t launch_write(const WriteParams &p, int in_dtype, int cache_dtype, int sm_count, int ctas_per_sm,
+                         cudaStream_t st) {
   const bool fp8 = cache_dtype == PA_FP8_E4M3;
+  const int c = ctas_per_sm;
   switch (in_dtype) {
-    case PA_F32: return fp8 ? launch_one<PA_F32, true>(p, sm_count, st) : launch_one<PA_F32, false>(p, sm_count, st);
-    case PA_BF16: return fp8 ? launch_one<PA_BF16, true>(p, sm_count, st) : launch_one<PA_BF16, false>(p, sm_count, st);
-    case PA_F16: return fp8 ? launch_one<PA_F16, true>(p, sm_count, st) : launch_one<PA_F16, false>(p, sm_count, st);
+    case PA_F32: return fp8 ? launch_one<PA_F32, true>(p, sm_count, c, st) : launch_one<PA_F32, false>(p, sm_count, c, st);
+    case PA_BF16: return fp8 ? launch_one<PA_BF16, true>(p, sm_count, c, st) : launch_one<PA_BF16, false>(p, sm_count, c, st);
+    case PA_F16: return fp8 ? launch_one<PA_F16, true>(p, sm_count, c, st) : launch_one<PA_F16, false>(p, sm_count, c, st);
     default: return cudaErrorInvalidValue;
   }
 }
