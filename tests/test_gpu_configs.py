@@ -200,6 +200,27 @@ def test_c5_fp8_write_and_sampled_decode():
     assert_close(got, step(st, -1), "c5 split vs unsplit")
 
 
+def test_c5_step_equals_two_calls():
+    """c5 through pa_decode_step (8192 new rows: the write on the grid it gets beside an early-
+    reading decode, many tokens per thread) against the write and the decode called one after
+    the other (checked against the oracle above): both caches and every output bit for bit."""
+    w = configs.get("c5")
+    a, b = bench.stage(w), bench.stage(w)
+    assert isinstance(b.new_rows_start, torch.Tensor)  # pa_decode_step with early reads
+    _, _, ws_a = bench.workspace_for(a, 0)
+    _, _, ws_b = bench.workspace_for(b, 0)
+    bench.run_write(a)
+    bench.run_decode(a, 0, ws_a)
+    bench.run_step(b, 0, ws_b)
+    torch.cuda.synchronize()
+    for st in (a, b):
+        rc, bits = pa.pa_check_device_error(st.err)
+        assert rc == 0, (rc, bits)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.k_cache.view(torch.uint8), b.k_cache.view(torch.uint8))
+    assert torch.equal(a.v_cache.view(torch.uint8), b.v_cache.view(torch.uint8))
+
+
 # ---------------------------------------- variants: NHD layout, ALiBi, per-head scales
 
 def test_c2_nhd_full_and_equal_to_hnd():
