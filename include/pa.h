@@ -295,7 +295,7 @@ int pa_decode_opt(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, 
  * query columns as Hq * max_query_len heads: pa_decode_plan / pa_decode_workspace_size
  * with num_heads = Hq * max_query_len give them.  PA_PARTITION_BALANCED is refused
  * (PA_ERR_UNSUPPORTED_SHAPE).  Kernels: with fewer than 64 query columns per KV head
- * (max_query_len * Hq / Hkv), an fp8 or fp32 cache, D other than 64 / 128, or a split
+ * (max_query_len * Hq / Hkv; 32 at head size 64), an fp8 or fp32 cache, D other than 64 / 128, or a split
  * asked for (partition_size > 0 or a cluster split), the decode kernels run with 8
  * columns per CTA, each CTA reading the pages its columns see.  Otherwise (bf16 / f16
  * cache, partition_size 0 or -1) a query-tile kernel runs on the tcgen05 tensor cores:

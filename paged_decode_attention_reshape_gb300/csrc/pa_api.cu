@@ -565,7 +565,7 @@ int decode_impl(pa_tensor *out, const pa_tensor *q, const pa_tensor *k_cache, co
   // Chunks of query tokens run on the query-tile kernel (rows in the MMA M dimension, pages
   // shared by 64 rows, no split) unless a split was asked for.
   const bool chunk = varlen && (kind == KIND_BF16 || kind == KIND_F16) && (D == 64 || D == 128) &&
-                     (partition_size == 0 || partition_size == -1) && VH >= kChunkMinColumns;
+                     (partition_size == 0 || partition_size == -1) && VH >= chunk_min_columns(D);
   const Plan pl = make_plan(S, Hqv, Hkv, D, maxNB, kind, sm, true, chunk ? -1 : partition_size);
   if (pl.status != PA_OK) return pl.status;
   const int P = pl.P;

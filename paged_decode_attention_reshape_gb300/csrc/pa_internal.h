@@ -158,8 +158,9 @@ cudaError_t launch_decode_f32(const DecodeParams &p, cudaStream_t st);
 cudaError_t launch_chunk_umma(const DecodeParams &p, int kind, const CUtensorMap &tmK, const CUtensorMap &tmV,
                               const CUtensorMap &tmQ, cudaStream_t st);
 // Query columns per KV head (max_query_len x G) from which varlen attention uses it: below
-// 64 columns the column-group kernels are as fast or faster.
-constexpr int kChunkMinColumns = 64;
+// that the column-group kernels are as fast or faster (256 sequences of 512-4096 tokens, 32/8
+// heads: at 32 columns 644 vs 737 us at head size 128, but 453 vs 325 us at head size 64).
+constexpr int chunk_min_columns(int D) { return D == 64 ? 32 : 64; }
 // Query columns per KV head above which the query-tile kernel takes two 128-row tiles per
 // CTA (head size 128).
 constexpr int kChunkTwoTileColumns = 128;

@@ -85,7 +85,7 @@ def test_decode_one_poll_limit_gives_untouched_or_correct_rows(P):
 
 @pytest.mark.parametrize("D", [128, 64])
 def test_query_tile_wait_that_runs_out_writes_nothing_and_recovers(D):
-    """pa_attention_varlen on the tcgen05 query-tile kernel (>= 64 query columns per KV head):
+    """pa_attention_varlen on the tcgen05 query-tile kernel (>= 64 query columns per KV head, 32 at D = 64):
     the MMA issuer's first K/V-group wait gives up, every role leaves, the copies and MMAs in
     flight are waited for, the tensor memory is freed, nothing is written."""
     v = make_varlen([700, 300, 129], [128, 40, 129], 32, 8, D, seed=900 + D)

@@ -229,6 +229,26 @@ def test_long_chunks_match_oracle(shape):
     assert_close(outs[64].double().cpu().numpy(), outs[-1].double().cpu().numpy(), "split 64 vs unsplit")
 
 
+def test_query_tile_at_32_columns_head_size_64():
+    """Head size 64 switches to the query tile at 32 query columns per KV head (8 new tokens x
+    G = 4): one partly filled 128-row tile per KV head, against the oracle and against the
+    column-group kernels (a split asked for)."""
+    lens, nqs = [300, 129, 40, 1000, 8], [8, 8, 5, 8, 8]
+    v = make_varlen(lens, nqs, 32, 8, 64, seed=51)
+    assert v.nq_max * 4 == 32
+    ref = reference(v)
+    g = on_gpu(v)
+    outs = {}
+    for P in (-1, 64):
+        got = run(v, g, P)
+        rc, bits = pa.pa_check_device_error(g.err)
+        assert rc == 0, (P, rc, bits)
+        outs[P] = got.double().cpu().numpy()
+        assert not np.isnan(outs[P]).any(), P
+        assert_close(outs[P], ref, "32 columns, partition %d" % P)
+    assert_close(outs[64], outs[-1], "column groups vs query tile")
+
+
 def test_query_tile_bad_ranges_are_reported_and_skipped():
     lens = [50, 40, 30]
     v = make_varlen(lens, [3, 17, 2], 32, 8, 64, seed=33, nq_max=16)  # 64 columns; sequence 1 > nq_max

@@ -132,9 +132,10 @@ class Workload:
 
     def query_tile(self) -> bool:
         """True when attention runs on the query-tile tensor-core kernel: 64 or more query
-        columns (new tokens x G) per KV head, a 16-bit cache, head size 64 or 128."""
-        return (self.nq > 1 and self.nq * self.G >= 64 and self.cache_dtype in ("bf16", "f16")
-                and self.D in (64, 128))
+        columns (new tokens x G) per KV head (32 at head size 64), a 16-bit cache, head size
+        64 or 128."""
+        return (self.nq > 1 and self.nq * self.G >= (32 if self.D == 64 else 64)
+                and self.cache_dtype in ("bf16", "f16") and self.D in (64, 128))
 
     def write_bytes(self) -> int:
         """Algorithmic bytes of one cache write: valid rows read and written, plus slot_mapping."""
