@@ -36,7 +36,7 @@
 // be a phase off); empty[slot] (one commit per active tile) -> TMA.  The MMAs
 // of one issuer run in order, so S of group k + 2 may overwrite the P that P.V of group k
 // reads.  Tile 0 zeroes the V rows past the sequence in the last page before it hands over
-// its P; the other tiles' last P.V also waits for that hand-over.
+// its P and arrives on v_tail (used once), which the other tiles' last P.V waits for.
 #pragma once
 
 #include "pa_device.cuh"
@@ -210,8 +210,8 @@ struct UmmaCfg {
   static constexpr int RING = R * BOXB;               // one box region of a ring
   static constexpr int QOFF = 0, KOFF = T * QTILE, VOFF = KOFF + NBOX * RING, BAR_OFF = VOFF + NBOX * RING;
   // barriers: full[NS], empty[NS]; per tile s_full x2, p_full x2, o_done, drain (48 bytes);
-  // q_full
-  static constexpr int TBAR = 2 * NS * 8, NBARS = 2 * NS + 6 * T + 1;
+  // q_full, v_tail
+  static constexpr int TBAR = 2 * NS * 8, NBARS = 2 * NS + 6 * T + 2;
   static constexpr size_t SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 256 * T;      // tile t: S/P buffers at 256 t + 0 / 64, O at 256 t + 128
   static constexpr uint32_t OCOL = 128;
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
   auto pfull = [&](int t, int b) { return tbar0 + 48u * t + 16u + 8u * b; };
   auto odone = [&](int t) { return tbar0 + 48u * t + 32u; };
   auto drain = [&](int t) { return tbar0 + 48u * t + 40u; };
-  const uint32_t qfull = tbar0 + 48u * T;
+  const uint32_t qfull = tbar0 + 48u * T, vtailb = qfull + 8u;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sgen + C::BAR_OFF + C::NBARS * 8);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *bad_block = reinterpret_cast<volatile int *>(tmem_slot + 2);
@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
       mbar_init(drain(t), 1);
     }
     mbar_init(qfull, 1);
+    mbar_init(vtailb, 128);
     *abort = 0;
     *bad_block = 0;
     fence_barrier_init();
@@ -420,11 +421,10 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
           const int kp = k - 1, gsp = kp % C::NS, bp = kp & 1;
           const int npg = min(C::GP, npages - kp * C::GP);
           if (!__all_sync(0xffffffffu, umma_wait(pfull(t, bp), (kp >> 1) & 1, abort))) break;
-          // the last page's V tail is zeroed by tile 0 before it hands over its P: the other
-          // tiles' last P.V waits for that too (the final phase of tile 0's barrier)
-          if (t > 0 && kp == ngr - 1 && vtail &&
-              !__all_sync(0xffffffffu, umma_wait(pfull(0, bp), (kp >> 1) & 1, abort)))
-            break;
+          // the last page's V tail is zeroed by tile 0 before it hands over its P; the other
+          // tiles' last P.V waits for that on v_tail, a barrier used once (a parity wait on
+          // tile 0's p_full could pass a phase early if tile 0 ran several groups behind)
+          if (t > 0 && kp == ngr - 1 && vtail && !__all_sync(0xffffffffu, umma_wait(vtailb, 0, abort))) break;
           umma::fence_after();
           if (elect_one()) {
             for (int i = 0; i < npg; ++i) {
@@ -563,6 +563,7 @@ __global__ void __launch_bounds__(UmmaCfg<KIND, D, T>::THREADS, UmmaCfg<KIND, D,
                 make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
+          mbar_arrive(vtailb);
         }
       }
       umma::fence_before();
